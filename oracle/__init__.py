@@ -1,0 +1,159 @@
+"""Float64 CPU oracle for the selective-scan hot path (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package. The CUDA library and its Python
+binding never import it; the two share no code. The arithmetic lives in
+``oracle.c`` (plain sequential loops in double precision); this module only
+builds that file with gcc and marshals numpy arrays to it.
+
+Inputs are the exact values the GPU is given: float32 arrays, or bf16 bit
+patterns widened exactly to float32 by ``workloads.bf16_bits_to_f32``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+          "-fPIC", "-shared", "-pthread"]
+
+
+def build(src: str = _SRC, out: str = _LIB, force: bool = False) -> str:
+    """Compile ``src`` to the shared library ``out`` with gcc (no fast-math,
+    no FMA contraction). Returns the path of the library."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, src, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle library."""
+    global _lib
+    with _lock:
+        if path is not None:
+            return _bind(ctypes.CDLL(path))
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    f = ctypes.POINTER(ctypes.c_float)
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
+    lib.oracle_affine_f64.argtypes = [f, f, dp, i64]
+    lib.oracle_affine_f64.restype = None
+    lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
+    lib.oracle_softplus_f64.restype = ctypes.c_double
+    s6 = [f, f, f, f, f, f, dp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int]
+    lib.oracle_s6_fwd_f64.argtypes = s6
+    lib.oracle_s6_fwd_f64.restype = ctypes.c_int
+    lib.oracle_s6_bidir_f64.argtypes = s6
+    lib.oracle_s6_bidir_f64.restype = ctypes.c_int
+    lib.oracle_s6_channels_f64.argtypes = [
+        f, f, f, f, f, f, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+        ctypes.POINTER(ctypes.c_int64), i64, dp, ctypes.c_int]
+    lib.oracle_s6_channels_f64.restype = ctypes.c_int
+    return lib
+
+
+def _f32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.float32:
+        raise TypeError(f"oracle inputs are float32 (got {a.dtype})")
+    return a
+
+
+def _p(a, t=ctypes.c_float):
+    return a.ctypes.data_as(ctypes.POINTER(t))
+
+
+# ---------------------------------------------------------------- affine
+def affine(a, b, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """h[t] = a[t]*h[t-1] + b[t], h[-1] = 0, in float64."""
+    lib = lib or load()
+    a, b = _f32(a), _f32(b)
+    if a.shape != b.shape or a.ndim != 1:
+        raise ValueError("a and b must be 1-D of equal length")
+    h = np.empty(a.shape[0], dtype=np.float64)
+    lib.oracle_affine_f64(_p(a), _p(b), _p(h, ctypes.c_double), a.shape[0])
+    return h
+
+
+def softplus(v: float, lib: ctypes.CDLL | None = None) -> float:
+    return (lib or load()).oracle_softplus_f64(float(v))
+
+
+# ---------------------------------------------------------------- S6
+def _s6_args(x, delta, Bt, Ct, A, Dskip):
+    x, delta, Bt, Ct, A = map(_f32, (x, delta, Bt, Ct, A))
+    B, L, D = x.shape
+    N = A.shape[1]
+    if delta.shape != (B, L, D) or Bt.shape != (B, L, N) or Ct.shape != (B, L, N):
+        raise ValueError("shape mismatch")
+    if A.shape != (D, N):
+        raise ValueError("A must be (D, N)")
+    Dskip = np.zeros(D, np.float32) if Dskip is None else _f32(Dskip)
+    if Dskip.shape != (D,):
+        raise ValueError("Dskip must be (D,)")
+    return x, delta, Bt, Ct, A, Dskip, B, L, D, N
+
+
+def s6_fwd(x, delta, Bt, Ct, A, Dskip=None, softplus=False, threads=1,
+           lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """S6 selective-scan forward, y (B, L, D) float64."""
+    lib = lib or load()
+    x, delta, Bt, Ct, A, Dskip, B, L, D, N = _s6_args(x, delta, Bt, Ct, A, Dskip)
+    y = np.zeros((B, L, D), dtype=np.float64)
+    rc = lib.oracle_s6_fwd_f64(_p(x), _p(delta), _p(Bt), _p(Ct), _p(A), _p(Dskip),
+                               _p(y, ctypes.c_double), B, L, D, N,
+                               int(bool(softplus)), int(threads))
+    if rc:
+        raise RuntimeError(f"oracle_s6_fwd_f64 failed ({rc})")
+    return y
+
+
+def s6_bidir(x, delta, Bt, Ct, A, Dskip=None, softplus=False, threads=1,
+             lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Forward plus reverse recurrence over shared dA, dBx; y (B, L, D)."""
+    lib = lib or load()
+    x, delta, Bt, Ct, A, Dskip, B, L, D, N = _s6_args(x, delta, Bt, Ct, A, Dskip)
+    y = np.zeros((B, L, D), dtype=np.float64)
+    rc = lib.oracle_s6_bidir_f64(_p(x), _p(delta), _p(Bt), _p(Ct), _p(A), _p(Dskip),
+                                 _p(y, ctypes.c_double), B, L, D, N,
+                                 int(bool(softplus)), int(threads))
+    if rc:
+        raise RuntimeError(f"oracle_s6_bidir_f64 failed ({rc})")
+    return y
+
+
+def s6_channels(x, delta, Bt, Ct, A, Dskip, chans, softplus=False, bidir=False,
+                threads=1, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """y for the listed channels c = b*D + d only, as (len(chans), L)."""
+    lib = lib or load()
+    x, delta, Bt, Ct, A, Dskip, B, L, D, N = _s6_args(x, delta, Bt, Ct, A, Dskip)
+    ch = np.ascontiguousarray(chans, dtype=np.int64)
+    out = np.zeros((ch.shape[0], L), dtype=np.float64)
+    rc = lib.oracle_s6_channels_f64(
+        _p(x), _p(delta), _p(Bt), _p(Ct), _p(A), _p(Dskip), B, L, D, N,
+        int(bool(softplus)), int(bool(bidir)), _p(ch, ctypes.c_int64),
+        ch.shape[0], _p(out, ctypes.c_double), int(threads))
+    if rc:
+        raise RuntimeError(f"oracle_s6_channels_f64 failed ({rc})")
+    return out

@@ -1,0 +1,226 @@
+/*
+ * Float64 CPU oracle for the selective-scan hot path.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library. The CUDA library never
+ * links, includes or calls it, and this file shares no code with it.
+ *
+ * Every function below is the plain sequential definition, evaluated in
+ * double precision from the exact values the GPU is given (fp32, or bf16
+ * widened exactly to fp32 by the caller). There is no blocking, no
+ * reassociation and no fast-math: build with -O2 -ffp-contract=off.
+ *
+ * Sources (web pages on the selective scan):
+ *   [SSK]  "Selective-scan CUDA kernels" (persus.netlify.app), opening
+ *          paragraphs: the recurrence h[t] = a[t]*h[t-1] + b[t] and its
+ *          affine-pair scan form.
+ *   [S6]   "POPCORNBENCH FW-GLM-5-1 l2_p30" (arjun-banerjee.github.io),
+ *          forward-pass derivation: dA = exp(delta*A), dB = delta*B_t,
+ *          x_db = x*dB, h = dA*h + x_db, y_t = sum_n h*C_t, y + x*D; the
+ *          layouts x,delta,y (B,L,D), B_t,C_t (B,L,N), A (D,N), D (D);
+ *          softplus on delta via log(1 + exp(v)); h starts at zero.
+ *   [ARM]  "ARM-Scan - Optimized Mamba Selective-Scan Kernel"
+ *          (krithiksama.me), Approach and What broke: forward and reverse
+ *          recurrences share the discretisation, and the fused result must
+ *          equal the two scans run independently.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - h[-1] = 0 for the affine scan; h starts at 0 for S6 ([S6]).
+ *   - softplus uses threshold 20: v > 20 returns v (PyTorch's default).
+ *   - the reverse recurrence applies dA and dBx of the same time index:
+ *     h_rev[t] = dA[t]*h_rev[t+1] + dBx[t], i.e. the forward scan of the
+ *     time-reversed inputs, read back in original order.
+ *   - in the bidirectional output each direction carries its own D*x term.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* ------------------------------------------------------------------ affine */
+
+/* [SSK] h[t] = a[t]*h[t-1] + b[t], with h[-1] = 0. */
+void oracle_affine_f64(const float *a, const float *b, double *h, int64_t n)
+{
+    double state = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        state = (double)a[t] * state + (double)b[t];
+        h[t] = state;
+    }
+}
+
+/* ------------------------------------------------------------------ S6 */
+
+/* [S6] softplus(v) = log(1 + exp(v)); v > 20 returns v. */
+double oracle_softplus_f64(double v)
+{
+    if (v > 20.0)
+        return v;
+    return log1p(exp(v));
+}
+
+typedef struct {
+    const float *x, *delta, *Bt, *Ct, *A, *Dskip;
+    int64_t B, L, D, N;
+    int softplus;
+    int bidir;
+    const int64_t *chans;   /* channel c = b*D + d; NULL means all B*D */
+    int64_t nchan;
+    double *out;            /* chans != NULL: (nchan, L); else (B, L, D) */
+    int64_t begin, end;     /* range of channel slots this worker owns */
+} s6_job;
+
+/* One (b, d) channel, every state n, every step t ([S6] forward pass).
+ * Writes y[t] for t in [0, L) with stride `ystride`.
+ * With `bidir`, adds the reverse recurrence ([ARM]) over the same dA, dBx. */
+static void s6_channel(const s6_job *j, int64_t b, int64_t d, double *h,
+                       double *y, int64_t ystride)
+{
+    const int64_t L = j->L, D = j->D, N = j->N;
+    const double Dd = (double)j->Dskip[d];
+
+    /* forward: t = 0 .. L-1 */
+    for (int64_t n = 0; n < N; ++n)
+        h[n] = 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t xi = (b * L + t) * D + d;   /* x[b, t, d] */
+        const int64_t bi = (b * L + t) * N;       /* B_t[b, t, :] */
+        double dl = (double)j->delta[xi];
+        if (j->softplus)
+            dl = oracle_softplus_f64(dl);
+        const double xv = (double)j->x[xi];
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double dA = exp(dl * (double)j->A[d * N + n]);
+            const double dB = dl * (double)j->Bt[bi + n];
+            const double x_db = xv * dB;
+            h[n] = dA * h[n] + x_db;
+            acc += h[n] * (double)j->Ct[bi + n];
+        }
+        y[t * ystride] = acc + xv * Dd;
+    }
+    if (!j->bidir)
+        return;
+
+    /* reverse: t = L-1 .. 0, h_rev[t] = dA[t]*h_rev[t+1] + dBx[t] */
+    for (int64_t n = 0; n < N; ++n)
+        h[n] = 0.0;
+    for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t xi = (b * L + t) * D + d;
+        const int64_t bi = (b * L + t) * N;
+        double dl = (double)j->delta[xi];
+        if (j->softplus)
+            dl = oracle_softplus_f64(dl);
+        const double xv = (double)j->x[xi];
+        double acc = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            const double dA = exp(dl * (double)j->A[d * N + n]);
+            const double dB = dl * (double)j->Bt[bi + n];
+            const double x_db = xv * dB;
+            h[n] = dA * h[n] + x_db;
+            acc += h[n] * (double)j->Ct[bi + n];
+        }
+        y[t * ystride] += acc + xv * Dd;
+    }
+}
+
+static void *s6_worker(void *arg)
+{
+    const s6_job *j = (const s6_job *)arg;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(j->N > 0 ? j->N : 1));
+    if (!h)
+        return (void *)1;
+    for (int64_t s = j->begin; s < j->end; ++s) {
+        const int64_t c = j->chans ? j->chans[s] : s;
+        const int64_t b = c / j->D, d = c % j->D;
+        if (j->chans)
+            s6_channel(j, b, d, h, j->out + s * j->L, 1);
+        else
+            s6_channel(j, b, d, h, j->out + b * j->L * j->D + d, j->D);
+    }
+    free(h);
+    return NULL;
+}
+
+/* Splits the independent (b, d) channels over `threads` POSIX threads.
+ * The per-channel loop is the same whatever the split. Returns 0 on success. */
+static int s6_run(s6_job base, int threads)
+{
+    const int64_t total = base.chans ? base.nchan : base.B * base.D;
+    if (total <= 0 || base.L <= 0)
+        return 0;
+    if (threads < 1)
+        threads = 1;
+    if (threads > total)
+        threads = (int)total;
+    if (threads == 1) {
+        base.begin = 0;
+        base.end = total;
+        return s6_worker(&base) ? -1 : 0;
+    }
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)threads);
+    s6_job *jobs = (s6_job *)malloc(sizeof(s6_job) * (size_t)threads);
+    if (!tid || !jobs) {
+        free(tid);
+        free(jobs);
+        return -1;
+    }
+    int rc = 0, started = 0;
+    for (int i = 0; i < threads; ++i) {
+        jobs[i] = base;
+        jobs[i].begin = total * i / threads;
+        jobs[i].end = total * (i + 1) / threads;
+        if (pthread_create(&tid[i], NULL, s6_worker, &jobs[i]) != 0) {
+            rc = -1;
+            break;
+        }
+        ++started;
+    }
+    for (int i = 0; i < started; ++i) {
+        void *ret = NULL;
+        pthread_join(tid[i], &ret);
+        if (ret)
+            rc = -1;
+    }
+    free(tid);
+    free(jobs);
+    return rc;
+}
+
+/* [S6] forward pass over all channels; y is (B, L, D) float64. */
+int oracle_s6_fwd_f64(const float *x, const float *delta, const float *Bt,
+                      const float *Ct, const float *A, const float *Dskip,
+                      double *y, int64_t B, int64_t L, int64_t D, int64_t N,
+                      int softplus, int threads)
+{
+    s6_job j = {x, delta, Bt, Ct, A, Dskip, B, L, D, N, softplus, 0,
+                NULL, 0, y, 0, 0};
+    return s6_run(j, threads);
+}
+
+/* [ARM] forward plus reverse recurrence over shared dA, dBx; y is (B, L, D). */
+int oracle_s6_bidir_f64(const float *x, const float *delta, const float *Bt,
+                        const float *Ct, const float *A, const float *Dskip,
+                        double *y, int64_t B, int64_t L, int64_t D, int64_t N,
+                        int softplus, int threads)
+{
+    s6_job j = {x, delta, Bt, Ct, A, Dskip, B, L, D, N, softplus, 1,
+                NULL, 0, y, 0, 0};
+    return s6_run(j, threads);
+}
+
+/* Selected channels only (c = b*D + d); out is (nchan, L) float64.
+ * Used to check full-size GPU outputs channel by channel. */
+int oracle_s6_channels_f64(const float *x, const float *delta, const float *Bt,
+                           const float *Ct, const float *A, const float *Dskip,
+                           int64_t B, int64_t L, int64_t D, int64_t N,
+                           int softplus, int bidir, const int64_t *chans,
+                           int64_t nchan, double *out, int threads)
+{
+    for (int64_t i = 0; i < nchan; ++i)
+        if (chans[i] < 0 || chans[i] >= B * D)
+            return -2;
+    s6_job j = {x, delta, Bt, Ct, A, Dskip, B, L, D, N, softplus, bidir,
+                chans, nchan, out, 0, 0};
+    return s6_run(j, threads);
+}

@@ -1,0 +1,330 @@
+"""Checks that pin the float64 oracle to facts fixed outside the oracle.
+
+Each check takes a loaded oracle library (ctypes handle) and raises
+AssertionError on a mismatch. The same checks run against the real oracle
+(tests/test_oracle_pins.py, all must pass) and against copies of oracle.c
+with a planted mistake (tests/test_oracle_mutants.py, at least one must
+fail), so a dropped term, a wrong sign or index, or a swapped operand in
+the oracle cannot go unnoticed.
+
+What pins what:
+  affine  a == 1 with integer b: the exact integer prefix sum.
+          a == 0: h == b exactly.
+          constant a, b == 1: geometric closed form (1 - a^(t+1)) / (1 - a).
+          constant a, general b: explicit power sum with math.fsum.
+          random dyadic inputs, n <= 8: every bracketing of the affine-pair
+          combine (a, b) o (a', b') = (a a', a' b + b') in exact rational
+          arithmetic equals the oracle exactly; the operand-swapped combine
+          does not.
+          impulse response: b = e_j gives products of a.
+  S6      explicit O(L^2) solution of the linear recurrence (matrix form),
+          with math.fsum, for forward and bidirectional outputs.
+          A == 0: prefix-sum closed form.  Ct == 0 or delta == 0: y == D x.
+          L == 1: one-step closed form.  softplus: ln 2 at 0, the identity
+          sp(v) - sp(-v) = v, threshold reading v > 20 -> v.
+          time-reversal involution of the bidirectional output; bidir equals
+          forward plus flipped forward of flipped inputs; linearity in x;
+          channel permutation equivariance; batch independence.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+
+
+# ---------------------------------------------------------------- helpers
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _dyadic(g, n, lo, hi, bits):
+    """Random multiples of 2**-bits in [lo, hi], exactly representable."""
+    k = g.integers(int(lo * 2 ** bits), int(hi * 2 ** bits) + 1, size=n)
+    return (k / 2.0 ** bits).astype(np.float32)
+
+
+def _combine(p, q):
+    """(a, b) o (a', b') = (a a', a' b + b'): p earlier, q later."""
+    return (p[0] * q[0], q[0] * p[1] + q[1])
+
+
+def _swapped(p, q):
+    return (p[0] * q[0], p[0] * q[1] + p[1])
+
+
+def _all_folds(items, comb):
+    """Every full bracketing of a non-empty sequence under `comb`."""
+    if len(items) == 1:
+        return [items[0]]
+    out = []
+    for k in range(1, len(items)):
+        for left in _all_folds(items[:k], comb):
+            for right in _all_folds(items[k:], comb):
+                out.append(comb(left, right))
+    return out
+
+
+def _rel(x, ref):
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(x - ref) / np.maximum(1.0, np.abs(ref)))) if x.size else 0.0
+
+
+# ---------------------------------------------------------------- affine pins
+def pin_affine_ones_integer(lib):
+    g = _rng(1)
+    n = 4096
+    b = g.integers(-8, 9, size=n).astype(np.float32)
+    a = np.ones(n, np.float32)
+    h = oracle.affine(a, b, lib=lib)
+    exact = np.cumsum(b.astype(np.int64))
+    assert np.array_equal(h, exact.astype(np.float64)), "a==1 must give the exact prefix sum"
+
+
+def pin_affine_zero(lib):
+    g = _rng(2)
+    b = g.standard_normal(1000).astype(np.float32)
+    h = oracle.affine(np.zeros_like(b), b, lib=lib)
+    assert np.array_equal(h, b.astype(np.float64)), "a==0 must give h==b"
+
+
+def pin_affine_geometric(lib):
+    for a0 in (0.5, 0.9, 0.99):
+        a32 = np.float32(a0)
+        n = 300
+        h = oracle.affine(np.full(n, a32, np.float32), np.ones(n, np.float32), lib=lib)
+        av = float(a32)
+        t = np.arange(n)
+        closed = (1.0 - av ** (t + 1)) / (1.0 - av)
+        assert _rel(h, closed) < 1e-12, f"geometric closed form, a={a0}"
+
+
+def pin_affine_power_sum(lib):
+    g = _rng(3)
+    n = 64
+    a32 = np.float32(0.875)
+    b = g.standard_normal(n).astype(np.float32)
+    h = oracle.affine(np.full(n, a32, np.float32), b, lib=lib)
+    av = float(a32)
+    ref = [math.fsum(av ** (t - j) * float(b[j]) for j in range(t + 1)) for t in range(n)]
+    assert _rel(h, ref) < 1e-12, "power-sum closed form"
+
+
+def pin_affine_bracketings(lib):
+    g = _rng(4)
+    for n in range(1, 8):
+        for _ in range(3):
+            a = _dyadic(g, n, -1.0, 1.0, 3)
+            b = _dyadic(g, n, -2.0, 2.0, 3)
+            h = oracle.affine(a, b, lib=lib)
+            pairs = [(Fraction(float(x)), Fraction(float(y))) for x, y in zip(a, b)]
+            for t in range(n):
+                for res in _all_folds(pairs[: t + 1], _combine):
+                    # h[t] is the b-part of the prefix composition (h[-1] = 0)
+                    assert Fraction(h[t]) == res[1], "bracketing disagrees with oracle"
+
+
+def pin_affine_swapped_combine_is_caught(lib):
+    """The suite must catch an operand-order error: the swapped combine gives
+    a different value on a random instance, so a scan built on it would fail
+    pin_affine_bracketings."""
+    g = _rng(5)
+    a = _dyadic(g, 6, -1.0, 1.0, 3)
+    b = _dyadic(g, 6, -2.0, 2.0, 3)
+    h = oracle.affine(a, b, lib=lib)
+    pairs = [(Fraction(float(x)), Fraction(float(y))) for x, y in zip(a, b)]
+    good = _all_folds(pairs, _combine)
+    bad = _all_folds(pairs, _swapped)
+    assert all(r[1] == Fraction(h[-1]) for r in good)
+    assert any(r[1] != Fraction(h[-1]) for r in bad), "swapped combine went unnoticed"
+
+
+def pin_affine_impulse(lib):
+    g = _rng(6)
+    n, j = 40, 7
+    a = _dyadic(g, n, 0.5, 1.0, 4)
+    b = np.zeros(n, np.float32)
+    b[j] = 1.0
+    h = oracle.affine(a, b, lib=lib)
+    for t in range(n):
+        ref = 0.0 if t < j else math.prod(float(v) for v in a[j + 1: t + 1])
+        assert abs(h[t] - ref) <= 1e-15 * max(1.0, abs(ref)), "impulse response"
+
+
+def pin_affine_edges(lib):
+    assert oracle.affine(np.zeros(0, np.float32), np.zeros(0, np.float32), lib=lib).shape == (0,)
+    h = oracle.affine(np.array([0.75], np.float32), np.array([-2.5], np.float32), lib=lib)
+    assert h[0] == -2.5
+
+
+AFFINE_PINS = [pin_affine_ones_integer, pin_affine_zero, pin_affine_geometric,
+               pin_affine_power_sum, pin_affine_bracketings,
+               pin_affine_swapped_combine_is_caught, pin_affine_impulse,
+               pin_affine_edges]
+
+
+# ---------------------------------------------------------------- S6 pins
+def _small_s6(seed, B=2, L=9, D=3, N=4, softplus=False, A_zero=False):
+    g = _rng(seed)
+    x = g.standard_normal((B, L, D)).astype(np.float32)
+    if softplus:
+        dl = g.normal(-1.0, 1.5, (B, L, D)).astype(np.float32)
+    else:
+        dl = (10.0 ** g.uniform(-2, 0, (B, L, D))).astype(np.float32)
+    Bt = g.standard_normal((B, L, N)).astype(np.float32)
+    Ct = g.standard_normal((B, L, N)).astype(np.float32)
+    # A depends on d and n, so a transposed index shows up
+    A = (np.zeros((D, N)) if A_zero else -g.uniform(0.2, 3.0, (D, N))).astype(np.float32)
+    Ds = g.standard_normal(D).astype(np.float32)
+    return x, dl, Bt, Ct, A, Ds
+
+
+def _sp(v):
+    return v if v > 20.0 else math.log1p(math.exp(v))
+
+
+def _matrix_form(x, dl, Bt, Ct, A, Ds, softplus, bidir):
+    """y[b,t,d] = sum_{j<=t} sum_n C[t,n] exp(A[d,n] sum_{i=j+1..t} delta_i)
+                  delta_j B[j,n] x_j + D x_t   (+ the mirror sum over j>=t)."""
+    B, L, D = x.shape
+    N = A.shape[1]
+    y = np.zeros((B, L, D))
+    for b in range(B):
+        for d in range(D):
+            dd = [(_sp(float(dl[b, t, d])) if softplus else float(dl[b, t, d])) for t in range(L)]
+            for t in range(L):
+                terms = []
+                for j in range(t + 1):
+                    s = math.fsum(dd[j + 1: t + 1])
+                    for n in range(N):
+                        terms.append(float(Ct[b, t, n]) * math.exp(float(A[d, n]) * s)
+                                     * dd[j] * float(Bt[b, j, n]) * float(x[b, j, d]))
+                if bidir:
+                    for j in range(t, L):
+                        s = math.fsum(dd[t:j])
+                        for n in range(N):
+                            terms.append(float(Ct[b, t, n]) * math.exp(float(A[d, n]) * s)
+                                         * dd[j] * float(Bt[b, j, n]) * float(x[b, j, d]))
+                    terms.append(float(Ds[d]) * float(x[b, t, d]))
+                terms.append(float(Ds[d]) * float(x[b, t, d]))
+                y[b, t, d] = math.fsum(terms)
+    return y
+
+
+def pin_s6_matrix_form(lib):
+    for seed, sp in ((10, False), (11, True)):
+        args = _small_s6(seed, softplus=sp)
+        y = oracle.s6_fwd(*args, softplus=sp, lib=lib)
+        ref = _matrix_form(*args, softplus=sp, bidir=False)
+        assert _rel(y, ref) < 1e-12, f"forward matrix form (softplus={sp})"
+
+
+def pin_s6_bidir_matrix_form(lib):
+    for seed, sp in ((12, False), (13, True)):
+        args = _small_s6(seed, L=8, softplus=sp)
+        y = oracle.s6_bidir(*args, softplus=sp, lib=lib)
+        ref = _matrix_form(*args, softplus=sp, bidir=True)
+        assert _rel(y, ref) < 1e-12, f"bidirectional matrix form (softplus={sp})"
+
+
+def pin_s6_A_zero(lib):
+    x, dl, Bt, Ct, A, Ds = _small_s6(14, L=50, A_zero=True)
+    y = oracle.s6_fwd(x, dl, Bt, Ct, A, Ds, lib=lib)
+    # dA = 1: h[t, n] = sum_{j<=t} delta_j B[j, n] x_j
+    u = dl.astype(np.float64) * x.astype(np.float64)                 # (B, L, D)
+    h = np.cumsum(u[:, :, :, None] * Bt.astype(np.float64)[:, :, None, :], axis=1)
+    ref = np.einsum("bldn,bln->bld", h, Ct.astype(np.float64)) + x * Ds.astype(np.float64)
+    assert _rel(y, ref) < 1e-12, "A == 0 prefix-sum closed form"
+
+
+def pin_s6_C_zero_and_delta_zero(lib):
+    x, dl, Bt, Ct, A, Ds = _small_s6(15, L=20)
+    ref = x.astype(np.float64) * Ds.astype(np.float64)
+    y = oracle.s6_fwd(x, dl, Bt, np.zeros_like(Ct), A, Ds, lib=lib)
+    assert np.array_equal(y, ref), "Ct == 0 must give y == D x"
+    y = oracle.s6_fwd(x, np.zeros_like(dl), Bt, Ct, A, Ds, lib=lib)
+    assert np.array_equal(y, ref), "delta == 0 must give y == D x"
+    y = oracle.s6_bidir(x, np.zeros_like(dl), Bt, Ct, A, Ds, lib=lib)
+    assert np.array_equal(y, 2.0 * ref), "bidir with delta == 0 gives 2 D x"
+
+
+def pin_s6_one_step(lib):
+    x, dl, Bt, Ct, A, Ds = _small_s6(16, L=1, N=5)
+    y = oracle.s6_fwd(x, dl, Bt, Ct, A, Ds, lib=lib)
+    B, _, D = x.shape
+    for b in range(B):
+        for d in range(D):
+            ref = math.fsum(float(Ct[b, 0, n]) * float(dl[b, 0, d]) * float(Bt[b, 0, n])
+                            * float(x[b, 0, d]) for n in range(5)) + float(Ds[d]) * float(x[b, 0, d])
+            assert abs(y[b, 0, d] - ref) <= 1e-14 * max(1.0, abs(ref)), "one-step closed form"
+
+
+def pin_softplus(lib):
+    sp = lambda v: oracle.softplus(v, lib=lib)
+    assert abs(sp(0.0) - math.log(2.0)) < 1e-16
+    for v in (-30.0, -5.0, -0.3, 0.7, 4.0, 19.5):
+        assert abs(sp(v) - sp(-v) - v) < 1e-14 * max(1.0, abs(v)), "sp(v) - sp(-v) = v"
+    assert sp(25.0) == 25.0 and sp(20.5) == 20.5, "threshold reading: v > 20 returns v"
+    assert abs(sp(-40.0) - math.exp(-40.0)) < 1e-30
+    assert abs(sp(1.0) - 1.3132616875182228) < 1e-15
+
+
+def pin_s6_reversal(lib):
+    args = _small_s6(17, L=30)
+    x, dl, Bt, Ct, A, Ds = args
+    y = oracle.s6_bidir(*args, lib=lib)
+    fl = lambda v: np.ascontiguousarray(v[:, ::-1])
+    yr = oracle.s6_bidir(fl(x), fl(dl), fl(Bt), fl(Ct), A, Ds, lib=lib)
+    assert np.array_equal(fl(yr), y), "bidir(flip(inputs)) == flip(bidir(inputs))"
+    yf = oracle.s6_fwd(*args, lib=lib)
+    yb = fl(oracle.s6_fwd(fl(x), fl(dl), fl(Bt), fl(Ct), A, Ds, lib=lib))
+    assert np.array_equal(y, yf + yb), "bidir == fwd + flip(fwd(flip))"
+
+
+def pin_s6_linear_in_x(lib):
+    x, dl, Bt, Ct, A, Ds = _small_s6(18, L=25)
+    x2 = _rng(19).standard_normal(x.shape).astype(np.float32)
+    for f in (oracle.s6_fwd, oracle.s6_bidir):
+        y1 = f(x, dl, Bt, Ct, A, Ds, lib=lib)
+        y2 = f(x2, dl, Bt, Ct, A, Ds, lib=lib)
+        y12 = f((x.astype(np.float64) + x2).astype(np.float32), dl, Bt, Ct, A, Ds, lib=lib)
+        # x + x2 is rounded to fp32; compare against the rounded-sum response
+        assert _rel(y12, y1 + y2) < 1e-6, "linearity in x"
+
+
+def pin_s6_channel_structure(lib):
+    x, dl, Bt, Ct, A, Ds = _small_s6(20, B=3, L=12, D=5)
+    y = oracle.s6_fwd(x, dl, Bt, Ct, A, Ds, lib=lib)
+    perm = np.array([3, 0, 4, 1, 2])
+    yp = oracle.s6_fwd(np.ascontiguousarray(x[:, :, perm]), np.ascontiguousarray(dl[:, :, perm]),
+                       Bt, Ct, np.ascontiguousarray(A[perm]), np.ascontiguousarray(Ds[perm]), lib=lib)
+    assert np.array_equal(yp, y[:, :, perm]), "channel permutation equivariance"
+    y0 = oracle.s6_fwd(x[:1], dl[:1], Bt[:1], Ct[:1], A, Ds, lib=lib)
+    assert np.array_equal(y0, y[:1]), "batch elements are independent"
+    ch = np.array([0, 7, 14, 3])
+    yc = oracle.s6_channels(x, dl, Bt, Ct, A, Ds, ch, lib=lib)
+    for i, c in enumerate(ch):
+        assert np.array_equal(yc[i], y[c // 5, :, c % 5]), "channel sampler agrees"
+
+
+S6_PINS = [pin_s6_matrix_form, pin_s6_bidir_matrix_form, pin_s6_A_zero,
+           pin_s6_C_zero_and_delta_zero, pin_s6_one_step, pin_softplus,
+           pin_s6_reversal, pin_s6_linear_in_x, pin_s6_channel_structure]
+
+ALL_PINS = AFFINE_PINS + S6_PINS
+
+
+def failures(lib) -> list[str]:
+    """Names of the pins that fail (or crash) for this oracle library."""
+    bad = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except Exception as e:  # noqa: BLE001 - any failure counts
+            bad.append(f"{pin.__name__}: {type(e).__name__}: {e}")
+    return bad

@@ -1,0 +1,9 @@
+"""The float64 oracle against facts fixed outside it (CPU only)."""
+import pytest
+
+import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(pin, oracle_lib):
+    pin(oracle_lib)
