@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan library on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input.
+The headline workload is the flat affine scan over n = 2**28 fp32 elements
+(a ~ U(0.9, 1), b ~ N(0, 1), seed 0): inputs are staged in HBM once, then K
+timed calls of ss_affine_scan follow W untimed ones. Inputs (3.2 GB with the
+output) are larger than L2, so no flush is needed between calls. The three
+S6 workloads are timed the same way (with an L2 flush between calls where
+their bytes fit in L2) and reported under "per_config".
+
+Rank 0 prints one JSON line. With --gpus N > 1 (under torchrun) every rank
+runs its own replica: the path has no exchange step, so there is no
+collective on the data path; value is the work of all ranks over the
+slowest rank's time.
+
+--impl reference times the float64 CPU oracle (the only reference this
+problem has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan elements/s, HBM GB/s and % of GB300 roofline (1 GPU)"
+HEADLINE = "affine_large"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_recurrences_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str, src_hash: str):
+    """dram bytes per launch from the committed ncu summary, or None when the
+    kernel changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = data.get(f"{kernel}/{workload}")
+    if not e or e.get("source_hash") != src_hash:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                         if r[3].replace(".", "").isdigit())}
+
+
+# ---------------------------------------------------------------- device timing
+def time_launches(torch, fn, steps, warmup, stream, flush=None, barrier=None):
+    """Per-launch CUDA-event durations (ms) of `fn` over `steps` timed calls,
+    plus the wall-to-wall event time of the whole timed region."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            if flush is not None:
+                flush()
+            fn()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        region0.record(stream)
+        for i in range(steps):
+            if flush is not None:
+                flush()
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+        region1.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, region0.elapsed_time(region1)
+
+
+def hbm_copy_probe(torch, dev):
+    """Sentinel: copy of 1 GiB (bf16), read + write bytes over the best time."""
+    a = torch.empty(1 << 29, dtype=torch.bfloat16, device=dev).fill_(1.0)
+    b = torch.empty_like(a)
+    best = None
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    del a, b
+    return 2 * (1 << 30) / (best * 1e-3) / 1e9
+
+
+def mufu_probe(torch, ss, dev, sms):
+    """ex2 operations per second on the special-function unit."""
+    blocks, iters = sms * 8, 4096
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    ss.ss_probe_mufu_ex2(out, blocks, iters)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ss.ss_probe_mufu_ex2(out, blocks, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    ops = blocks * 256 * 8 * iters
+    return ops / (best * 1e-3)
+
+
+# ---------------------------------------------------------------- workloads
+def affine_setup(torch, dev, name):
+    import workloads
+    w = workloads.AFFINE[name]
+    a, b = workloads.affine_inputs(w.n, w.a_lo, w.a_hi)
+    return w, a, b, torch.from_numpy(a).to(dev), torch.from_numpy(b).to(dev)
+
+
+def s6_bytes_and_ops(w):
+    es = 2 if w.io == "bf16" else 4
+    B, L, D, N = w.B, w.L, w.D, w.N
+    byts = 3 * es * B * L * D + 2 * es * B * L * N + 4 * D * N + 4 * D
+    mufu = B * L * D * N + (2 * B * L * D if w.softplus else 0)
+    return byts, mufu
+
+
+def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
+    import workloads
+    w = workloads.S6[name]
+    inp = workloads.s6_workload_inputs(w)
+
+    def t(v):
+        x = torch.from_numpy(v)
+        if inp.io == "bf16" and v.dtype.name == "uint16":
+            x = x.view(torch.bfloat16)
+        return x.to(dev)
+
+    args = (t(inp.x), t(inp.delta), t(inp.Bt), t(inp.Ct), t(inp.A), t(inp.Dskip))
+    y = torch.empty_like(args[0])
+    fn = ss.ss_selective_scan_bidir if w.bidir else ss.ss_selective_scan_fwd
+    call = lambda: fn(*args, delta_softplus=w.softplus, y=y, stream=stream)
+    byts, mufu = s6_bytes_and_ops(w)
+    flush = None
+    if byts < 2 * L2_BYTES:
+        junk = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = lambda: junk.fill_(0.0)
+    per, _ = time_launches(torch, call, steps, warmup, stream, flush=flush)
+    ms = statistics.mean(per)
+    t_hbm = byts / (hbm_peak * 1e9)
+    t_sfu = mufu / sfu_peak
+    t_roof = max(t_hbm, t_sfu)
+    return {
+        "elements": w.elements, "shape": [w.B, w.L, w.D, w.N], "io": w.io,
+        "softplus": w.softplus, "bidir": w.bidir, "ms": ms, "ms_min": min(per),
+        "elements_per_s": w.elements / (ms * 1e-3),
+        "gbs": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts, "mufu_ops": mufu,
+        "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6,
+        "bound": "hbm" if t_hbm >= t_sfu else "sfu",
+        "roofline_frac": t_roof / (ms * 1e-3),
+        "l2": "flushed between calls" if flush else "inputs larger than L2",
+        "workspace_bytes": ss.ss_selective_scan_workspace_bytes(
+            w.B, w.L, w.D, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32, w.bidir),
+    }
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import workloads
+    w = workloads.AFFINE[HEADLINE]
+    sample = 1 << 27
+    a, b = workloads.affine_inputs(sample, w.a_lo, w.a_hi)
+    lib = oracle.load()
+    for _ in range(max(args.warmup, 0)):
+        oracle.affine(a[: 1 << 20], b[: 1 << 20], lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        h = oracle.affine(a, b, lib=lib)
+    dt = time.perf_counter() - t0
+    assert np.isfinite(h[-1])
+    value = sample * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "elements/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE, "n_per_step": sample, "n_workload": w.n,
+                   "a": "U(0.9,1)", "b": "N(0,1)", "seed": 0},
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first 2**27 of the {HEADLINE} inputs per step, "
+                                   "sequential float64 loop, one thread"},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(budget_s: float):
+    """The oracle as it stands, on the headline input, on this host."""
+    import oracle
+    import workloads
+    w = workloads.AFFINE[HEADLINE]
+    a, b = workloads.affine_inputs(w.n, w.a_lo, w.a_hi)
+    lib = oracle.load()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.affine(a, b, lib=lib)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s or reps >= 20:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": w.n * reps / dt, "unit": "elements/s", "cores": 1, "kind": "oracle",
+            "sample": f"full {HEADLINE} input (2**28 elements) x {reps} passes, sequential "
+                      "float64 loop, one thread"}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import linear_recurrences_gb300 as ss
+    from linear_recurrences_gb300 import build as ssbuild
+    ssbuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        barrier = dist.barrier
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+
+    w, a_np, b_np, a, b = affine_setup(torch, dev, HEADLINE)
+    h = torch.empty_like(a)
+    ws = ss.new_workspace(ss.ss_affine_scan_workspace_bytes(w.n), dev)
+    call = lambda: ss.ss_affine_scan(a, b, h, workspace=ws, stream=stream)
+
+    with ClockSampler(local_rank) as clk:
+        per, region_ms = time_launches(torch, call, args.steps, args.warmup, stream,
+                                       barrier=barrier)
+    status = ss.ss_get_device_status(ws, stream)
+    if status != ss.SS_OK:
+        raise RuntimeError(f"device reported {ss.ss_status_string(status)}")
+    clocks = clk.summary()
+    region_ms_all = region_ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([region_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        region_ms_all = float(t.item())
+    elems = w.n * args.steps * world
+    value = elems / (region_ms_all * 1e-3)
+    launch_ms = statistics.mean(per)
+    alg_bytes = 12 * w.n
+    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+    src = source_hash("affine_scan.cu", "ss_common.cuh")
+
+    # end to end through the C ABI with host buffers: H2D inputs, scan, D2H output
+    a_host = torch.from_numpy(a_np).pin_memory()
+    b_host = torch.from_numpy(b_np).pin_memory()
+    h_host = torch.empty(w.n, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        a.copy_(a_host, non_blocking=True)
+        b.copy_(b_host, non_blocking=True)
+        ss.ss_affine_scan(a, b, h, workspace=ws, stream=stream)
+        h_host.copy_(h, non_blocking=True)
+
+    e2e_per, e2e_region = time_launches(torch, e2e_step, max(3, args.steps // 4),
+                                        min(args.warmup, 3), stream, barrier=barrier)
+    e2e_value = w.n * len(e2e_per) * world / (e2e_region * 1e-3)
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        sfu = mufu_probe(torch, ss, dev, sms)
+        extras["sfu_probe_ex2_per_s"] = sfu
+        if clocks.get("sm_mhz"):
+            extras["sfu_probe_ex2_per_clk_per_sm"] = sfu / (clocks["sm_mhz"] * 1e6) / sms
+        extras["hbm_probe_gbs"] = hbm_copy_probe(torch, dev)
+        per_cfg = {}
+        small_w, *_rest, sa, sb = affine_setup(torch, dev, "affine_small")
+        sh = torch.empty_like(sa)
+        sws = ss.new_workspace(ss.ss_affine_scan_workspace_bytes(small_w.n), dev)
+        junk = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        sper, _ = time_launches(torch, lambda: ss.ss_affine_scan(sa, sb, sh, workspace=sws,
+                                                                 stream=stream),
+                                args.steps, args.warmup, stream, flush=lambda: junk.fill_(0.0))
+        del junk
+        sms_ = statistics.mean(sper)
+        per_cfg["affine_small"] = {"elements": small_w.n, "ms": sms_,
+                                   "elements_per_s": small_w.n / (sms_ * 1e-3),
+                                   "gbs": 12 * small_w.n / (sms_ * 1e-3) / 1e9,
+                                   "bound": "launch latency", "l2": "flushed between calls"}
+        per_cfg[HEADLINE] = {"elements": w.n, "ms": launch_ms,
+                             "elements_per_s": w.n / (launch_ms * 1e-3), "gbs": achieved,
+                             "bound": "hbm", "roofline_frac": achieved / hbm_peak}
+        for name in ("s6_fp32", "s6_bf16", "s6_bidir"):
+            per_cfg[name] = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream,
+                                     hbm_peak, sfu)
+        extras["per_config"] = per_cfg
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": region_ms_all / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": HEADLINE, "n": w.n, "a": "U(0.9,1)", "b": "N(0,1)", "seed": 0,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (3.2 GB per call), no flush"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": committed_traffic("affine_scan_kernel", HEADLINE, src),
+                     "kernel": "affine_scan_kernel", "algorithmic_bytes_per_launch": alg_bytes,
+                     "avg_launch_ms": launch_ms},
+        "cpu_baseline": cpu_baseline(args.cpu_seconds) if world == 1 else None,
+        "e2e": {"value": e2e_value, "unit": "elements/s", "h2d_bytes_per_step": 8 * w.n,
+                "d2h_bytes_per_step": 4 * w.n},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "source_hash": src,
+    }
+    line.update(extras)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

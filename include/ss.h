@@ -1,0 +1,164 @@
+/*
+ * ss.h - C ABI of the GB300 selective-scan library (libss.so).
+ *
+ * The library computes, on one NVIDIA GB300 GPU (sm_103a), the first-order
+ * affine recurrence and the Mamba S6 selective-scan forward built on it:
+ *
+ *   affine scan   h[t] = a[t] * h[t-1] + b[t],  h[-1] = 0
+ *                 ("Selective-scan CUDA kernels", persus.netlify.app, opening
+ *                 paragraphs: the recurrence is a prefix scan over affine
+ *                 pairs, associative but not commutative)
+ *
+ *   S6 forward    delta' = softplus(delta) if requested, else delta
+ *                 dA  = exp(delta' * A[d, n])
+ *                 dBx = delta' * Bt[b, t, n] * x[b, t, d]
+ *                 h[n] = dA * h[n] + dBx,  h starts at 0
+ *                 y[b, t, d] = sum_n h[n] * Ct[b, t, n] + Dskip[d] * x[b, t, d]
+ *                 ("POPCORNBENCH FW-GLM-5-1 l2_p30", arjun-banerjee.github.io,
+ *                 forward-pass derivation and kernel layouts)
+ *
+ *   S6 bidir      y = forward output + output of the reverse recurrence
+ *                 h_rev[n] = dA[t] * h_rev[n] + dBx[t] run from t = L-1 down
+ *                 to 0 over the same dA, dBx, each direction with its own
+ *                 Dskip * x term ("ARM-Scan", krithiksama.me, Approach: the
+ *                 two directions share the discretisation; What broke: the
+ *                 fused result equals the two scans run independently).
+ *
+ * Conventions for every call:
+ *  - Pointers named a, b, h, x, delta, Bt, Ct, A, Dskip, y and workspace are
+ *    DEVICE pointers owned by the caller. The library allocates nothing and
+ *    frees nothing.
+ *  - Tensors are dense and row-major: x, delta, y are (B, L, D) with element
+ *    (b, t, d) at b*L*D + t*D + d; Bt, Ct are (B, L, N) with (b, t, n) at
+ *    (b*L + t)*N + n; A is (D, N); Dskip is (D,). Any 4-byte (fp32) or
+ *    2-byte (bf16) aligned pointer is accepted; 16-byte aligned rows take the
+ *    vectorised load path.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *    asynchronous on that stream and return once the work is enqueued.
+ *  - The workspace is scratch device memory of at least the size the
+ *    matching *_workspace_bytes() call returns, 256-byte aligned. It must be
+ *    zero-filled (cudaMemset) before its first use and before it is used
+ *    for a different entry point or a different S6 shape; between calls of
+ *    the same entry point and shape the kernels leave it ready for the next
+ *    call. Calls that may run at the same time on the GPU need distinct
+ *    workspaces. Results are bitwise reproducible from call to call.
+ *  - Argument errors are returned synchronously, with nothing launched.
+ *    A failed launch returns SS_ERR_CUDA. Errors the GPU detects while
+ *    running (a look-back wait that exceeded the spin timeout) are recorded
+ *    in the workspace and returned by ss_get_device_status().
+ *  - Sizes of zero (n == 0, or B, L or D == 0) are valid and launch nothing.
+ */
+#ifndef SS_H
+#define SS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SS_ABI_VERSION 1
+
+/* Storage type of x, delta, Bt, Ct and y. State and arithmetic are fp32. */
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+typedef enum {
+    SS_OK = 0,
+    SS_ERR_INVALID = 1,      /* null pointer, negative size, bad dtype       */
+    SS_ERR_UNSUPPORTED = 2,  /* N outside [1, 16], or a size above a limit   */
+    SS_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned   */
+    SS_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed         */
+    SS_ERR_TIMEOUT = 5,      /* a device-side wait exceeded the spin timeout */
+    SS_ERR_BOUNDS = 6        /* a device-side index check failed             */
+} ss_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *ss_status_string(int status);
+
+/* SS_ABI_VERSION of the loaded library. */
+int ss_abi_version(void);
+
+/* ------------------------------------------------------------ affine scan */
+
+/* Bytes of workspace ss_affine_scan needs for n elements (0 for n <= 0). */
+size_t ss_affine_scan_workspace_bytes(int64_t n);
+
+/*
+ * h[t] = a[t] * h[t-1] + b[t] for t in [0, n), h[-1] = 0, all fp32.
+ * ("Selective-scan CUDA kernels", persus.netlify.app: the recurrence and its
+ * single-pass decoupled look-back scan.)
+ * a, b: n input floats each; h: n output floats (may alias neither input).
+ * One launch: tiles of 4096 elements staged into shared memory by bulk
+ * copies, a register and warp-shuffle scan inside each tile, and a
+ * decoupled look-back across tiles whose fold order makes the result
+ * independent of scheduling.
+ */
+ss_status ss_affine_scan(const float *a, const float *b, float *h, int64_t n,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------ S6 */
+
+/* Bytes of workspace the S6 calls need for this shape and storage type on
+ * the current device (bidir != 0 for ss_selective_scan_bidir). 0 when the
+ * call needs none, in which case workspace may be NULL. */
+size_t ss_selective_scan_workspace_bytes(int64_t B, int64_t L, int64_t D,
+                                         int64_t N, int io_dtype, int bidir);
+
+/*
+ * S6 selective-scan forward (see the top of this file for the arithmetic).
+ * x, delta: (B, L, D); Bt, Ct: (B, L, N); y: (B, L, D), all of `io_dtype`.
+ * A: (D, N) fp32 (already negative, e.g. -exp(A_log)); Dskip: (D,) fp32 or
+ * NULL for no skip term. delta_softplus != 0 applies softplus(v) =
+ * log(1 + exp(v)) to delta in the kernel (v > 20 passes v through).
+ * 1 <= N <= 16. y must not alias an input.
+ * Long sequences are split into chunks over L whose carries are exchanged by
+ * a decoupled look-back; short ones run one register-resident chain per
+ * (b, d, n) group over all of L.
+ */
+ss_status ss_selective_scan_fwd(const void *x, const void *delta,
+                                const void *Bt, const void *Ct,
+                                const float *A, const float *Dskip, void *y,
+                                int64_t B, int64_t L, int64_t D, int64_t N,
+                                int io_dtype, int delta_softplus,
+                                void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
+ * Bidirectional S6: y = forward output + time-reversed output, with dA and
+ * dBx computed from the same delta, x, Bt (same arguments as
+ * ss_selective_scan_fwd). Runs chunked over L with a forward look-back and
+ * a reverse look-forward; every chunk of one (b, d-tile) sequence must be
+ * resident at once, which the call checks against the GPU's occupancy
+ * (SS_ERR_UNSUPPORTED if L is too long for that).
+ */
+ss_status ss_selective_scan_bidir(const void *x, const void *delta,
+                                  const void *Bt, const void *Ct,
+                                  const float *A, const float *Dskip, void *y,
+                                  int64_t B, int64_t L, int64_t D, int64_t N,
+                                  int io_dtype, int delta_softplus,
+                                  void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/* ------------------------------------------------------------ errors */
+
+/*
+ * Synchronises `stream`, then reads and clears the error word the kernels
+ * keep in `workspace` (SS_OK if nothing went wrong since the last call).
+ * SS_ERR_CUDA if the synchronisation itself fails.
+ */
+ss_status ss_get_device_status(void *workspace, void *stream);
+
+/*
+ * Upper bound, in nanoseconds, on any single device-side wait in later
+ * launches (default 1e9 = 1 s). A wait that runs out records SS_ERR_TIMEOUT
+ * in the workspace and the kernel finishes without hanging.
+ * SS_ERR_INVALID for 0.
+ */
+ss_status ss_set_spin_timeout_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SS_H */

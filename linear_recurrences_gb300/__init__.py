@@ -1,0 +1,270 @@
+"""Python binding of the GB300 selective-scan library (libss.so, include/ss.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI. PyTorch provides device memory and streams.
+There is no CPU fallback: if the library was not built, or no CUDA device is
+present, the calls raise.
+
+Functions keep the C names:
+  ss_affine_scan(a, b, h=None, workspace=None, stream=None) -> h
+  ss_selective_scan_fwd(x, delta, Bt, Ct, A, Dskip=None, delta_softplus=False, y=None, ...)
+  ss_selective_scan_bidir(...same...)
+  ss_get_device_status(workspace, stream=None) -> status code
+plus workspace helpers. Tensors must be contiguous CUDA tensors: fp32 for the
+affine scan; fp32 or bf16 (all of x, delta, Bt, Ct, y alike) for S6, with A
+and Dskip fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "SS_OK", "SS_ERR_INVALID", "SS_ERR_UNSUPPORTED", "SS_ERR_WORKSPACE", "SS_ERR_CUDA",
+    "SS_ERR_TIMEOUT", "SS_ERR_BOUNDS", "SS_F32", "SS_BF16", "SSError", "lib", "library_path",
+    "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
+    "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
+    "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
+    "ss_probe_mufu_ex2", "new_workspace", "EXPORTED_SYMBOLS",
+]
+
+SS_OK, SS_ERR_INVALID, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
+SS_ERR_CUDA, SS_ERR_TIMEOUT, SS_ERR_BOUNDS = 4, 5, 6
+SS_F32, SS_BF16 = 0, 1
+
+EXPORTED_SYMBOLS = (
+    "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
+    "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
+    "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
+    "ss_probe_mufu_ex2",
+)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_DEFAULT_LIB = os.path.join(_PKG, "_build", "libss.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class SSError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {ss_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return os.environ.get("SS_LIBRARY", _DEFAULT_LIB)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libss.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libss.so not found at {path}; build it with "
+                    "`python -m linear_recurrences_gb300.build`")
+            _lib = _bind(ctypes.CDLL(path))
+        return _lib
+
+
+def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
+    vp, i64, sz, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    L.ss_status_string.argtypes = [ci]
+    L.ss_status_string.restype = ctypes.c_char_p
+    L.ss_abi_version.argtypes = []
+    L.ss_abi_version.restype = ci
+    L.ss_affine_scan_workspace_bytes.argtypes = [i64]
+    L.ss_affine_scan_workspace_bytes.restype = sz
+    L.ss_affine_scan.argtypes = [vp, vp, vp, i64, vp, sz, vp]
+    L.ss_affine_scan.restype = ci
+    L.ss_selective_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, ci, ci]
+    L.ss_selective_scan_workspace_bytes.restype = sz
+    s6 = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ci, ci, vp, sz, vp]
+    L.ss_selective_scan_fwd.argtypes = s6
+    L.ss_selective_scan_fwd.restype = ci
+    L.ss_selective_scan_bidir.argtypes = s6
+    L.ss_selective_scan_bidir.restype = ci
+    L.ss_get_device_status.argtypes = [vp, vp]
+    L.ss_get_device_status.restype = ci
+    L.ss_set_spin_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.ss_set_spin_timeout_ns.restype = ci
+    L.ss_testing_skip_publish_once.argtypes = [i64]
+    L.ss_testing_skip_publish_once.restype = None
+    L.ss_probe_mufu_ex2.argtypes = [vp, ci, ci, vp]
+    L.ss_probe_mufu_ex2.restype = ci
+    return L
+
+
+def ss_status_string(status: int) -> str:
+    try:
+        return lib().ss_status_string(int(status)).decode()
+    except RuntimeError:
+        return str(status)
+
+
+def ss_abi_version() -> int:
+    return lib().ss_abi_version()
+
+
+def ss_set_spin_timeout_ns(ns: int) -> None:
+    st = lib().ss_set_spin_timeout_ns(int(ns))
+    if st != SS_OK:
+        raise SSError(st, "ss_set_spin_timeout_ns")
+
+
+def ss_testing_skip_publish_once(unit: int) -> None:
+    """Test hook (include/ss_testing.h): the next launch lets work unit `unit`
+    skip publishing its look-back descriptors, so waits on it time out."""
+    lib().ss_testing_skip_publish_once(int(unit))
+
+
+def ss_probe_mufu_ex2(out, blocks: int, iters: int, stream=None) -> None:
+    """Measurement kernel (include/ss_probe.h): blocks*256*8*iters MUFU ex2 ops."""
+    sh = _stream_handle(stream, out.device)
+    st = lib().ss_probe_mufu_ex2(_ptr(out), int(blocks), int(iters), sh)
+    if st != SS_OK:
+        raise SSError(st, "ss_probe_mufu_ex2")
+
+
+# ---------------------------------------------------------------- torch glue
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(t, name, dtypes):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() > 0 else 0)
+
+
+_ws_cache: dict = {}
+
+
+def new_workspace(nbytes: int, device):
+    """A zero-filled, 256-byte aligned device workspace of at least nbytes."""
+    torch = _torch()
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _cached_workspace(key, nbytes, device, stream_handle):
+    """One zeroed workspace per (entry point, shape, device, stream), reused
+    across calls as the C ABI allows."""
+    full = (key, str(device), stream_handle.value)
+    ws = _ws_cache.get(full)
+    if ws is None or ws.numel() < nbytes:
+        ws = new_workspace(nbytes, device)
+        _ws_cache[full] = ws
+    return ws
+
+
+def ss_affine_scan_workspace_bytes(n: int) -> int:
+    return lib().ss_affine_scan_workspace_bytes(int(n))
+
+
+def ss_affine_scan(a, b, h=None, workspace=None, stream=None):
+    """h[t] = a[t]*h[t-1] + b[t] (fp32, 1-D, on the GPU). Returns h."""
+    torch = _torch()
+    _check_cuda(a, "a", (torch.float32,))
+    _check_cuda(b, "b", (torch.float32,))
+    if a.dim() != 1 or a.shape != b.shape or a.device != b.device:
+        raise ValueError("a and b must be 1-D, same length, same device")
+    n = a.numel()
+    if h is None:
+        h = torch.empty_like(a)
+    _check_cuda(h, "h", (torch.float32,))
+    if h.shape != a.shape:
+        raise ValueError("h must match a")
+    sh = _stream_handle(stream, a.device)
+    need = ss_affine_scan_workspace_bytes(n)
+    if workspace is None and need:
+        workspace = _cached_workspace(("affine",), need, a.device, sh)
+    wsb = workspace.numel() if workspace is not None else 0
+    st = lib().ss_affine_scan(_ptr(a), _ptr(b), _ptr(h), n, _ptr(workspace), wsb, sh)
+    if st != SS_OK:
+        raise SSError(st, "ss_affine_scan")
+    return h
+
+
+def ss_selective_scan_workspace_bytes(B, L, D, N, io_dtype=SS_F32, bidir=False) -> int:
+    return lib().ss_selective_scan_workspace_bytes(int(B), int(L), int(D), int(N),
+                                                   int(io_dtype), int(bool(bidir)))
+
+
+def _s6(fn_name, x, delta, Bt, Ct, A, Dskip, delta_softplus, y, workspace, stream, bidir):
+    torch = _torch()
+    io = (torch.float32, torch.bfloat16)
+    for t, nm in ((x, "x"), (delta, "delta"), (Bt, "Bt"), (Ct, "Ct")):
+        _check_cuda(t, nm, io)
+    if not (x.dtype == delta.dtype == Bt.dtype == Ct.dtype):
+        raise TypeError("x, delta, Bt, Ct must share one dtype")
+    _check_cuda(A, "A", (torch.float32,))
+    if Dskip is not None:
+        _check_cuda(Dskip, "Dskip", (torch.float32,))
+    if x.dim() != 3 or A.dim() != 2:
+        raise ValueError("x must be (B, L, D) and A (D, N)")
+    B, L, D = x.shape
+    N = A.shape[1]
+    if delta.shape != x.shape or Bt.shape != (B, L, N) or Ct.shape != (B, L, N) or A.shape[0] != D:
+        raise ValueError("shape mismatch between x, delta, Bt, Ct, A")
+    if Dskip is not None and Dskip.shape != (D,):
+        raise ValueError("Dskip must be (D,)")
+    if y is None:
+        y = torch.empty_like(x)
+    _check_cuda(y, "y", (x.dtype,))
+    if y.shape != x.shape:
+        raise ValueError("y must match x")
+    io_dtype = SS_BF16 if x.dtype == torch.bfloat16 else SS_F32
+    sh = _stream_handle(stream, x.device)
+    need = ss_selective_scan_workspace_bytes(B, L, D, N, io_dtype, bidir)
+    if workspace is None and need:
+        key = (fn_name, B, L, D, N, io_dtype, need, os.environ.get("SS_S6_WT_TSUB"))
+        workspace = _cached_workspace(key, need, x.device, sh)
+    wsb = workspace.numel() if workspace is not None else 0
+    st = getattr(lib(), fn_name)(_ptr(x), _ptr(delta), _ptr(Bt), _ptr(Ct), _ptr(A), _ptr(Dskip),
+                                 _ptr(y), B, L, D, N, io_dtype, int(bool(delta_softplus)),
+                                 _ptr(workspace), wsb, sh)
+    if st != SS_OK:
+        raise SSError(st, fn_name)
+    return y
+
+
+def ss_selective_scan_fwd(x, delta, Bt, Ct, A, Dskip=None, delta_softplus=False, y=None,
+                          workspace=None, stream=None):
+    """S6 selective-scan forward; returns y (B, L, D) in x's dtype."""
+    return _s6("ss_selective_scan_fwd", x, delta, Bt, Ct, A, Dskip, delta_softplus, y,
+               workspace, stream, False)
+
+
+def ss_selective_scan_bidir(x, delta, Bt, Ct, A, Dskip=None, delta_softplus=False, y=None,
+                            workspace=None, stream=None):
+    """Bidirectional S6 (forward + time-reversed over shared dA, dBx)."""
+    return _s6("ss_selective_scan_bidir", x, delta, Bt, Ct, A, Dskip, delta_softplus, y,
+               workspace, stream, True)
+
+
+def ss_get_device_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns (then clears) the device error word."""
+    dev = workspace.device if workspace is not None else None
+    sh = _stream_handle(stream, dev)
+    return lib().ss_get_device_status(_ptr(workspace), sh)

@@ -1,0 +1,133 @@
+// C ABI of libss.so: argument validation, workspace checks, dispatch.
+// The arithmetic lives in affine_scan.cu and s6_scan.cu.
+#include <atomic>
+#include <cstdint>
+
+#include "ss_common.cuh"
+#include "ss_internal.h"
+#include "ss_testing.h"
+
+namespace {
+
+std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
+std::atomic<long long> g_skip_unit{-1};
+
+// Consumes a pending ss_testing_skip_publish_once request (-1 if none).
+long long take_skip_unit() { return g_skip_unit.exchange(-1); }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ss_status s6_entry(const void *x, const void *delta, const void *Bt, const void *Ct, const float *A,
+                   const float *Dskip, void *y, int64_t B, int64_t L, int64_t D, int64_t N,
+                   int io_dtype, int delta_softplus, void *workspace, size_t workspace_bytes,
+                   void *stream, int bidir) {
+    if (B < 0 || L < 0 || D < 0 || N < 0) return SS_ERR_INVALID;
+    if (io_dtype != SS_F32 && io_dtype != SS_BF16) return SS_ERR_INVALID;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0 || D == 0) return SS_OK;
+    if (!x || !delta || !Bt || !Ct || !A || !y) return SS_ERR_INVALID;
+    const uintptr_t es = io_dtype == SS_BF16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(delta, es) || !aligned(Bt, es) || !aligned(Ct, es) ||
+        !aligned(y, es) || !aligned(A, 4) || (Dskip && !aligned(Dskip, 4)))
+        return SS_ERR_INVALID;
+    if (B > (1LL << 31) || L > (1LL << 40) || D > (1LL << 31) || B * L > (1LL << 48))
+        return SS_ERR_UNSUPPORTED;
+    ss::S6Args a;
+    a.x = x;
+    a.delta = delta;
+    a.Bt = Bt;
+    a.Ct = Ct;
+    a.A = A;
+    a.Dskip = Dskip;
+    a.y = y;
+    a.B = B;
+    a.L = L;
+    a.D = D;
+    a.N = N;
+    a.io_bf16 = io_dtype == SS_BF16;
+    a.softplus = delta_softplus != 0;
+    a.bidir = bidir;
+    return ss::s6_launch(a, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                         g_timeout_ns.load(), take_skip_unit());
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ss_status_string(int status) {
+    switch (status) {
+        case SS_OK: return "SS_OK";
+        case SS_ERR_INVALID: return "SS_ERR_INVALID";
+        case SS_ERR_UNSUPPORTED: return "SS_ERR_UNSUPPORTED";
+        case SS_ERR_WORKSPACE: return "SS_ERR_WORKSPACE";
+        case SS_ERR_CUDA: return "SS_ERR_CUDA";
+        case SS_ERR_TIMEOUT: return "SS_ERR_TIMEOUT";
+        case SS_ERR_BOUNDS: return "SS_ERR_BOUNDS";
+        default: return "SS_ERR_UNKNOWN";
+    }
+}
+
+int ss_abi_version(void) { return SS_ABI_VERSION; }
+
+size_t ss_affine_scan_workspace_bytes(int64_t n) { return ss::affine_workspace_bytes(n); }
+
+ss_status ss_affine_scan(const float *a, const float *b, float *h, int64_t n, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    if (n < 0) return SS_ERR_INVALID;
+    if (n == 0) return SS_OK;
+    if (!a || !b || !h) return SS_ERR_INVALID;
+    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(h, 4)) return SS_ERR_INVALID;
+    const size_t need = ss::affine_workspace_bytes(n);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SS_ERR_WORKSPACE;
+    return ss::affine_launch(a, b, h, n, workspace, static_cast<cudaStream_t>(stream),
+                             g_timeout_ns.load(), take_skip_unit());
+}
+
+size_t ss_selective_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,
+                                         int bidir) {
+    if (N < 1 || N > 16 || (io_dtype != SS_F32 && io_dtype != SS_BF16)) return 0;
+    return ss::s6_workspace_bytes(B, L, D, N, io_dtype == SS_BF16, bidir != 0);
+}
+
+ss_status ss_selective_scan_fwd(const void *x, const void *delta, const void *Bt, const void *Ct,
+                                const float *A, const float *Dskip, void *y, int64_t B, int64_t L,
+                                int64_t D, int64_t N, int io_dtype, int delta_softplus,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    return s6_entry(x, delta, Bt, Ct, A, Dskip, y, B, L, D, N, io_dtype, delta_softplus, workspace,
+                    workspace_bytes, stream, 0);
+}
+
+ss_status ss_selective_scan_bidir(const void *x, const void *delta, const void *Bt, const void *Ct,
+                                  const float *A, const float *Dskip, void *y, int64_t B, int64_t L,
+                                  int64_t D, int64_t N, int io_dtype, int delta_softplus,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    return s6_entry(x, delta, Bt, Ct, A, Dskip, y, B, L, D, N, io_dtype, delta_softplus, workspace,
+                    workspace_bytes, stream, 1);
+}
+
+ss_status ss_get_device_status(void *workspace, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SS_ERR_CUDA;
+    if (!workspace) return SS_OK;
+    ss::WsHeader *ws = static_cast<ss::WsHeader *>(workspace);
+    unsigned err = 0;
+    if (cudaMemcpy(&err, &ws->error, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SS_ERR_CUDA;
+    if (err != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(&ws->error, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return SS_ERR_CUDA;
+    }
+    return static_cast<ss_status>(err);
+}
+
+void ss_testing_skip_publish_once(int64_t unit) { g_skip_unit.store(unit < 0 ? -1 : unit); }
+
+ss_status ss_set_spin_timeout_ns(uint64_t ns) {
+    if (ns == 0) return SS_ERR_INVALID;
+    g_timeout_ns.store(ns);
+    return SS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,30 @@
+// Internal launch entry points shared by the C-ABI translation unit.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ss.h"
+
+namespace ss {
+
+size_t affine_workspace_bytes(int64_t n);
+ss_status affine_launch(const float *a, const float *b, float *h, int64_t n, void *workspace,
+                        cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit);
+
+struct S6Args {
+    const void *x, *delta, *Bt, *Ct;
+    const float *A, *Dskip;
+    void *y;
+    int64_t B, L, D, N;
+    int io_bf16;
+    int softplus;
+    int bidir;
+};
+
+size_t s6_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir);
+ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStream_t stream,
+                    unsigned long long timeout_ns, long long skip_unit);
+
+}  // namespace ss

@@ -1,0 +1,96 @@
+"""The C ABI library: loads without a GPU, exports what include/ss.h
+declares, and rejects bad arguments synchronously (no launch, no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_recurrences_gb300 as ss
+from linear_recurrences_gb300 import build as ssbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INCLUDE = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def L():
+    ssbuild.build()
+    return ss.lib()
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(INCLUDE):
+        if f.endswith(".h"):
+            text = open(os.path.join(INCLUDE, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(ss_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("ss_affine_scan", "ss_selective_scan_fwd", "ss_selective_scan_bidir"):
+        assert required in names
+    assert set(names) == set(ss.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} not exported by libss.so"
+
+
+def test_status_strings(L):
+    assert ss.ss_status_string(ss.SS_OK) == "SS_OK"
+    assert ss.ss_status_string(ss.SS_ERR_TIMEOUT) == "SS_ERR_TIMEOUT"
+    assert ss.ss_status_string(99) == "SS_ERR_UNKNOWN"
+    assert L.ss_abi_version() == 1
+
+
+def test_affine_argument_errors(L):
+    p = ctypes.c_void_p(256)  # never dereferenced: every call below fails validation
+    assert L.ss_affine_scan(p, p, p, -1, p, 1 << 20, None) == ss.SS_ERR_INVALID
+    assert L.ss_affine_scan(None, p, p, 10, p, 1 << 20, None) == ss.SS_ERR_INVALID
+    assert L.ss_affine_scan(ctypes.c_void_p(258), p, p, 10, p, 1 << 20, None) == ss.SS_ERR_INVALID
+    assert L.ss_affine_scan(p, p, p, 10, None, 0, None) == ss.SS_ERR_WORKSPACE
+    assert L.ss_affine_scan(p, p, p, 10000, p, 64, None) == ss.SS_ERR_WORKSPACE
+    assert L.ss_affine_scan(p, p, p, 0, None, 0, None) == ss.SS_OK  # empty: nothing to do
+
+
+def test_affine_workspace_size(L):
+    assert L.ss_affine_scan_workspace_bytes(0) == 0
+    assert L.ss_affine_scan_workspace_bytes(1) == 256 + 32
+    assert L.ss_affine_scan_workspace_bytes(4096) == 256 + 32
+    assert L.ss_affine_scan_workspace_bytes(4097) == 256 + 64
+    assert L.ss_affine_scan_workspace_bytes(1 << 28) == 256 + 32 * 65536
+
+
+def test_s6_argument_errors(L):
+    p = ctypes.c_void_p(256)
+    args = lambda B, L_, D, N, io=0, sp=0, ws=None, wsb=0: (
+        p, p, p, p, p, None, p, B, L_, D, N, io, sp, ws, wsb, None)
+    for fn in (L.ss_selective_scan_fwd, L.ss_selective_scan_bidir):
+        assert fn(*args(2, 8, 4, 17)) == ss.SS_ERR_UNSUPPORTED
+        assert fn(*args(2, 8, 4, 0)) == ss.SS_ERR_UNSUPPORTED
+        assert fn(*args(-1, 8, 4, 16)) == ss.SS_ERR_INVALID
+        assert fn(*args(2, 8, 4, 16, io=7)) == ss.SS_ERR_INVALID
+        assert fn(*args(0, 8, 4, 16)) == ss.SS_OK
+        assert fn(*args(2, 0, 4, 16)) == ss.SS_OK
+        bad = (None, p, p, p, p, None, p, 2, 8, 4, 16, 0, 0, None, 0, None)
+        assert fn(*bad) == ss.SS_ERR_INVALID
+    assert L.ss_selective_scan_workspace_bytes(2, 8, 4, 17, 0, 0) == 0
+
+
+def test_spin_timeout(L):
+    assert L.ss_set_spin_timeout_ns(0) == ss.SS_ERR_INVALID
+    assert L.ss_set_spin_timeout_ns(10**9) == ss.SS_OK
+
+
+def test_product_path_never_touches_the_oracle():
+    pkg = os.path.join(ROOT, "linear_recurrences_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f"{f} mentions the oracle"

@@ -1,0 +1,179 @@
+"""GPU S6 forward and bidirectional scans vs the float64 oracle."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_util import rel_err, require_gpu, to_dev, to_host_f64
+
+pytestmark = pytest.mark.gpu
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return require_gpu()
+
+
+@pytest.fixture(scope="module")
+def ss():
+    import linear_recurrences_gb300 as m
+    return m
+
+
+@pytest.fixture
+def plan_override():
+    """Sets the S6 tuning override (warps per CTA, timesteps per warp) for one test."""
+    old = os.environ.get("SS_S6_WT_TSUB")
+
+    def set_(wt, tsub):
+        os.environ["SS_S6_WT_TSUB"] = f"{wt},{tsub}"
+    yield set_
+    if old is None:
+        os.environ.pop("SS_S6_WT_TSUB", None)
+    else:
+        os.environ["SS_S6_WT_TSUB"] = old
+
+
+def gpu_run(ss, torch, inp, softplus, bidir):
+    dev = torch.device("cuda:0")
+    t = lambda v: to_dev(v, dev, inp.io)
+    fn = ss.ss_selective_scan_bidir if bidir else ss.ss_selective_scan_fwd
+    y = fn(t(inp.x), t(inp.delta), t(inp.Bt), t(inp.Ct), t(inp.A), t(inp.Dskip),
+           delta_softplus=softplus)
+    return to_host_f64(y)
+
+
+def oracle_run(inp, softplus, bidir):
+    f = oracle.s6_bidir if bidir else oracle.s6_fwd
+    return f(inp.x_f32, inp.delta_f32, inp.Bt_f32, inp.Ct_f32, inp.A, inp.Dskip,
+             softplus=softplus, threads=THREADS)
+
+
+def small(B, L, D, N, io="f32", softplus=False, seed=0, A_random=True):
+    inp = workloads.s6_inputs(B, L, D, N, io=io, delta="preact" if softplus else "loguniform",
+                              dskip="normal", seed=seed)
+    if A_random:  # d- and n-dependent A so a transposed index cannot hide
+        g = np.random.Generator(np.random.PCG64(seed + 100))
+        inp.A = (-g.uniform(0.1, 4.0, (D, N))).astype(np.float32)
+    return inp
+
+
+SHAPES = [
+    # (B, L, D, N)
+    (1, 1, 1, 1),
+    (2, 2, 3, 4),
+    (1, 33, 32, 16),
+    (2, 64, 33, 16),
+    (3, 100, 64, 8),
+    (2, 257, 40, 3),
+    (1, 1000, 96, 16),
+    (4, 513, 31, 5),
+]
+
+
+@pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
+@pytest.mark.parametrize("io,softplus", [("f32", False), ("f32", True), ("bf16", True), ("bf16", False)])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(torch, ss, shape, io, softplus, bidir):
+    inp = small(*shape, io=io, softplus=softplus, seed=sum(shape))
+    y = gpu_run(ss, torch, inp, softplus, bidir)
+    ref = oracle_run(inp, softplus, bidir)
+    assert rel_err(y, ref) <= TOL[io]
+
+
+@pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
+@pytest.mark.parametrize("wt,tsub", [(1, 1), (1, 7), (2, 8), (3, 5), (8, 4), (4, 33), (8, 64)])
+def test_chunk_splits(torch, ss, plan_override, wt, tsub, bidir):
+    """Forces many chunks and sub-chunks so the look-back, the look-forward
+    and the in-CTA folds run across ragged boundaries."""
+    plan_override(wt, tsub)
+    inp = small(2, 777, 70, 16, seed=wt * 100 + tsub)
+    y = gpu_run(ss, torch, inp, False, bidir)
+    assert rel_err(y, oracle_run(inp, False, bidir)) <= TOL["f32"]
+
+
+def test_chunked_bf16_softplus(torch, ss, plan_override):
+    plan_override(4, 16)
+    inp = small(3, 1500, 48, 16, io="bf16", softplus=True, seed=5)
+    for bidir in (False, True):
+        y = gpu_run(ss, torch, inp, True, bidir)
+        assert rel_err(y, oracle_run(inp, True, bidir)) <= TOL["bf16"]
+
+
+def test_null_dskip(torch, ss):
+    inp = small(2, 50, 16, 16, seed=9)
+    dev = torch.device("cuda:0")
+    t = lambda v: to_dev(v, dev)
+    y = ss.ss_selective_scan_fwd(t(inp.x), t(inp.delta), t(inp.Bt), t(inp.Ct), t(inp.A), None)
+    ref = oracle.s6_fwd(inp.x_f32, inp.delta_f32, inp.Bt_f32, inp.Ct_f32, inp.A, None)
+    assert rel_err(to_host_f64(y), ref) <= TOL["f32"]
+
+
+# ---------------------------------------------------------------- workloads
+def _sample_channels(B, D, count, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    chans = np.unique(np.concatenate([[0, B * D - 1, D - 1, D], g.integers(0, B * D, count)]))
+    return chans[chans < B * D]
+
+
+@pytest.mark.parametrize("name", ["s6_fp32", "s6_bf16", "s6_bidir"])
+def test_workload(torch, ss, name):
+    """Each S6 workload at full size, in the benchmark's launch configuration;
+    s6_fp32 is compared in full, the larger two on sampled channels."""
+    w = workloads.S6[name]
+    inp = workloads.s6_workload_inputs(w)
+    y = gpu_run(ss, torch, inp, w.softplus, w.bidir)
+    if name == "s6_fp32":
+        ref = oracle_run(inp, w.softplus, w.bidir)
+        assert rel_err(y, ref) <= TOL[w.io]
+        return
+    chans = _sample_channels(w.B, w.D, 160, seed=1)
+    ref = oracle.s6_channels(inp.x_f32, inp.delta_f32, inp.Bt_f32, inp.Ct_f32, inp.A, inp.Dskip,
+                             chans, softplus=w.softplus, bidir=w.bidir, threads=THREADS)
+    got = np.stack([y[c // w.D, :, c % w.D] for c in chans])
+    assert rel_err(got, ref) <= TOL[w.io]
+
+
+@pytest.mark.parametrize("name", ["s6_fp32", "s6_bf16", "s6_bidir"])
+def test_workload_determinism_1000_runs(torch, ss, name):
+    w = workloads.S6[name]
+    inp = workloads.s6_workload_inputs(w)
+    dev = torch.device("cuda:0")
+    t = lambda v: to_dev(v, dev, inp.io)
+    args = (t(inp.x), t(inp.delta), t(inp.Bt), t(inp.Ct), t(inp.A), t(inp.Dskip))
+    fn = ss.ss_selective_scan_bidir if w.bidir else ss.ss_selective_scan_fwd
+    first = fn(*args, delta_softplus=w.softplus).clone()
+    out = torch.empty_like(first)
+    for _ in range(1000):
+        fn(*args, delta_softplus=w.softplus, y=out)
+        assert torch.equal(out, first)
+
+
+@pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
+def test_timeout_is_reported_not_hung(torch, ss, plan_override, bidir):
+    """One chunk skips publishing; the bounded waits on it run out, the host
+    reads SS_ERR_TIMEOUT, and the next call on the same workspace is clean."""
+    plan_override(2, 16)
+    inp = small(2, 640, 64, 16, seed=21)
+    dev = torch.device("cuda:0")
+    t = lambda v: to_dev(v, dev)
+    args = (t(inp.x), t(inp.delta), t(inp.Bt), t(inp.Ct), t(inp.A), t(inp.Dskip))
+    fn = ss.ss_selective_scan_bidir if bidir else ss.ss_selective_scan_fwd
+    B, L, D, N = 2, 640, 64, 16
+    ws = ss.new_workspace(ss.ss_selective_scan_workspace_bytes(B, L, D, N, ss.SS_F32, bidir), dev)
+    out = torch.empty_like(args[0])
+    try:
+        ss.ss_set_spin_timeout_ns(5_000_000)
+        ss.ss_testing_skip_publish_once(7)
+        fn(*args, y=out, workspace=ws)
+        assert ss.ss_get_device_status(ws) == ss.SS_ERR_TIMEOUT
+    finally:
+        ss.ss_testing_skip_publish_once(-1)
+        ss.ss_set_spin_timeout_ns(1_000_000_000)
+    fn(*args, y=out, workspace=ws)
+    assert ss.ss_get_device_status(ws) == ss.SS_OK
+    assert rel_err(to_host_f64(out), oracle_run(inp, False, bidir)) <= TOL["f32"]
