@@ -417,6 +417,40 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_single(args):
+    """One workload's timed loop on this GPU (used for per-kernel timing and
+    for ncu captures); prints one JSON line for that workload."""
+    import torch
+    import workloads
+    import linear_recurrences_gb300 as ss
+    from linear_recurrences_gb300 import build as ssbuild
+    ssbuild.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    peaks, _ = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    name = args.workload
+    if name in workloads.S6:
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        sfu = mufu_probe(torch, ss, dev, sms) if not args.no_extras else 9.86e12
+        r = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream, hbm_peak, sfu)
+    elif name in workloads.AFFINE:
+        w, _, _, a, b = affine_setup(torch, dev, name)
+        if args.affine_n:
+            w = workloads.AffineWorkload(name, args.affine_n, w.a_lo, w.a_hi)
+            a, b = a[: w.n].contiguous(), b[: w.n].contiguous()
+        h = torch.empty_like(a)
+        ws = ss.new_workspace(ss.ss_affine_scan_workspace_bytes(w.n), dev)
+        per, _ = time_launches(torch, lambda: ss.ss_affine_scan(a, b, h, workspace=ws, stream=stream),
+                               args.steps, args.warmup, stream)
+        ms = statistics.mean(per)
+        r = {"elements": w.n, "ms": ms, "elements_per_s": w.n / (ms * 1e-3),
+             "gbs": 12 * w.n / (ms * 1e-3) / 1e9, "roofline_frac": 12 * w.n / (ms * 1e-3) / 1e9 / hbm_peak}
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    print(json.dumps({"workload": name, "steps": args.steps, "warmup": args.warmup, **r}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,6 +459,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--affine-n", type=int, default=0,
+                    help="with --workload affine_*: use this many elements (small ncu captures)")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="time one workload only (affine_small, affine_large, s6_fp32, "
+                         "s6_bf16, s6_bidir); the default is the full benchmark")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
@@ -433,6 +472,9 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.workload != HEADLINE or args.affine_n:
+        run_single(args)
         return
     if world > 1:
         import torch

@@ -8,8 +8,13 @@
 // one's discretisation. The pages' kernels (one thread per (b,d) running all
 // of L; a NEON/multicore CPU scan) are prior art; this file is a new design:
 //
-//  * lane = one channel d with NG of its N states in registers; a warp is
-//    32 consecutive channels, so x, delta and y accesses are coalesced;
+//  * lane = one channel d with NG of its N states in registers, updated
+//    two at a time with packed f32x2 fma/mul; a warp is 32 consecutive
+//    channels, so x, delta and y accesses are coalesced;
+//  * each warp streams its timesteps through a 3-slot shared-memory ring:
+//    one bulk async copy (cp.async.bulk) per x and delta row and one per
+//    B_t / C_t tile land on the slot's mbarrier while the warp computes on
+//    the slot two stages behind;
 //  * a CTA is WT warps that split one chunk of L into WT sub-chunks; a
 //    sequence (b, 32 channels) is split into K chunks, one CTA each;
 //  * with K == 1 and WT == 1 a warp runs its chains over all of L (the
@@ -42,9 +47,13 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kMaxWT = 8;       // warps per CTA along time
+constexpr int kMaxWT = 8;       // warps per CTA along time (hard limit)
+constexpr int kDefaultWT = 4;   // default: small CTAs so several fit per SM
 constexpr int kMaxWindows = 4;  // look-back holds up to 128 predecessor chunks
+constexpr int kTS = 8;          // timesteps per ring stage
+constexpr int kStages = 3;      // ring slots per warp
 constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned long long kCopyTimeoutNs = 2000000000ull;
 
 // Descriptor payload fields, each [32 lanes][NG] floats per (sequence, chunk).
 enum { F_P = 0, F_H = 1, F_INC = 2, F_HR = 3, F_RINC = 4 };
@@ -62,7 +71,7 @@ struct S6Params {
     int K;             // chunks per sequence
     int WT;            // warps per CTA
     int Tsub;          // timesteps per warp
-    int vecBC;         // Bt, Ct rows readable with 16-byte vector loads
+    int bulk;          // rows and tiles are 16-byte aligned: stage with bulk copies
     WsHeader *ws;
     unsigned *flags;   // [(seq*K + k)*4 + FL_*]
     float *payload;    // [((seq*K + k)*NF + field)*32*NG + lane*NG + i]
@@ -70,62 +79,39 @@ struct S6Params {
     long long skip_unit;  // test hook: this unit publishes nothing (-1: none)
 };
 
-// ------------------------------------------------------------------ io helpers
-template <typename IO> struct Io;
-template <> struct Io<float> {
-    static __device__ __forceinline__ float ld(const float *p) { return __ldg(p); }
-    static __device__ __forceinline__ void st(float *p, float v) { __stcs(p, v); }
-};
-template <> struct Io<__nv_bfloat16> {
-    static __device__ __forceinline__ float ld(const __nv_bfloat16 *p) {
-        return __bfloat162float(__ldg(p));
-    }
-    static __device__ __forceinline__ void st(__nv_bfloat16 *p, float v) {
-        *p = __float2bfloat16_rn(v);
-    }
-};
-
-__device__ __forceinline__ float bf16lo(unsigned w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
-
-// NG consecutive values of a (B, L, N) row starting at p (element g*NG).
-template <int NG, typename IO>
-__device__ __forceinline__ void load_states(const IO *p, int nvalid, bool vec, float (&v)[NG]) {
-    if (vec) {
-        if constexpr (sizeof(IO) == 4) {
-#pragma unroll
-            for (int q = 0; q < NG / 4; ++q) {
-                const float4 f = __ldg(reinterpret_cast<const float4 *>(p) + q);
-                v[4 * q + 0] = f.x;
-                v[4 * q + 1] = f.y;
-                v[4 * q + 2] = f.z;
-                v[4 * q + 3] = f.w;
-            }
-        } else if constexpr (NG % 8 == 0) {
-#pragma unroll
-            for (int q = 0; q < NG / 8; ++q) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4 *>(p) + q);
-                v[8 * q + 0] = bf16lo(w.x);
-                v[8 * q + 1] = bf16hi(w.x);
-                v[8 * q + 2] = bf16lo(w.y);
-                v[8 * q + 3] = bf16hi(w.y);
-                v[8 * q + 4] = bf16lo(w.z);
-                v[8 * q + 5] = bf16hi(w.z);
-                v[8 * q + 6] = bf16lo(w.w);
-                v[8 * q + 7] = bf16hi(w.w);
-            }
-        } else {
-            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(p));
-            v[0] = bf16lo(w.x);
-            v[1] = bf16hi(w.x);
-            v[2] = bf16lo(w.y);
-            v[3] = bf16hi(w.y);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < NG; ++i) v[i] = i < nvalid ? Io<IO>::ld(p + i) : 0.0f;
-    }
+// ------------------------------------------------------------------ f32x2
+typedef unsigned long long u64;
+__device__ __forceinline__ u64 f2(float lo, float hi) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
 }
+__device__ __forceinline__ float f2lo(u64 v) {
+    float lo;
+    asm("mov.b64 {%0, _}, %1;" : "=f"(lo) : "l"(v));
+    return lo;
+}
+__device__ __forceinline__ float f2hi(u64 v) {
+    float hi;
+    asm("mov.b64 {_, %0}, %1;" : "=f"(hi) : "l"(v));
+    return hi;
+}
+__device__ __forceinline__ u64 f2mul(u64 a, u64 b) {
+    u64 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ u64 f2fma(u64 a, u64 b, u64 c) {
+    u64 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// ------------------------------------------------------------------ io helpers
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ void store_io(float *p, float v) { __stcs(p, v); }
+__device__ __forceinline__ void store_io(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
 // softplus(v) = log(1 + exp(v)); v > 20 returns v. exp and log on MUFU; for
 // exp(v) < 1/64 the log is replaced by its alternating series so that the
@@ -147,7 +133,8 @@ template <int NG>
 __device__ __forceinline__ void store_field(float *dst, const float (&v)[NG]) {
 #pragma unroll
     for (int q = 0; q < NG / 4; ++q)
-        __stcg(reinterpret_cast<float4 *>(dst) + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        __stcg(reinterpret_cast<float4 *>(dst) + q,
+               make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
 }
 template <int NG>
 __device__ __forceinline__ void load_field(const float *src, float (&v)[NG]) {
@@ -170,88 +157,248 @@ __device__ __forceinline__ void publish_flag(const S6Params &p, long long unit, 
     if (lane == 0 && unit != p.skip_unit) st_release_u32(p.flags + unit * 4 + which, tag);
 }
 
-// ------------------------------------------------------------------ sweeps
-// One pass of this lane's chains over timesteps [t0, t1).
-// MODE_AGG: from a zero state, accumulate the sub-chunk aggregate.
-// MODE_OUT: from the state in h, write outputs.
+// ------------------------------------------------------------------ staging ring
+// Per-warp shared memory: kStages slots of {x rows, delta rows, Bt tile, Ct
+// tile} in the storage type, then fp32 copies of the current Bt / Ct rows
+// padded to 16 states (used for bf16 storage or N != NG).
+template <typename IO> struct Ring {
+    static constexpr int kXBytes = kTS * 32 * (int)sizeof(IO);
+    static constexpr int kBBytes = kTS * 16 * (int)sizeof(IO);
+    static constexpr int kSlot = 2 * kXBytes + 2 * kBBytes;
+    static constexpr int kConv = 2 * kTS * 16 * 4;
+    static constexpr int kWarp = kStages * kSlot + kConv;
+};
+
+struct WarpCtx {
+    unsigned char *ring;   // this warp's ring
+    uint64_t *bars;        // this warp's kStages mbarriers
+    unsigned issued;       // stage loads issued so far (all sweeps)
+    long long b, d0, d;
+    int cw;                // valid channels in this warp's tile
+    int lane;
+    bool dvalid;
+    long long t0, t1;      // this warp's timesteps
+};
+
 enum { MODE_AGG = 0, MODE_OUT = 1 };
 
-template <int NG, typename IO, bool SP, bool BIDIR, int MODE, bool REV>
-__device__ __forceinline__ void sweep(const S6Params &p, long long b, long long d, bool dvalid,
-                                      long long t0, long long t1, const float (&A2)[NG], float Dd,
-                                      float (&h)[NG], float (&hr)[NG], float (&Q)[NG], float &sdel,
-                                      float *yf, bool final_out) {
-    const IO *xp = static_cast<const IO *>(p.x);
-    const IO *dp = static_cast<const IO *>(p.delta);
-    const IO *bp = static_cast<const IO *>(p.Bt);
-    const IO *cp = static_cast<const IO *>(p.Ct);
-    const long long L = p.L, D = p.D;
+// Starts loading stage `st` (timesteps t0 + st*kTS ...) into `slot`.
+template <typename IO, int MODE>
+__device__ __forceinline__ void issue_stage(const S6Params &p, WarpCtx &w, int st, int slot) {
+    using R = Ring<IO>;
+    const long long ts = w.t0 + (long long)st * kTS;
+    const int nrows = (int)min((long long)kTS, w.t1 - ts);
+    unsigned char *sl = w.ring + slot * R::kSlot;
+    IO *xs = reinterpret_cast<IO *>(sl);
+    IO *ds = reinterpret_cast<IO *>(sl + R::kXBytes);
+    IO *bs = reinterpret_cast<IO *>(sl + 2 * R::kXBytes);
+    IO *cs = reinterpret_cast<IO *>(sl + 2 * R::kXBytes + R::kBBytes);
+    const IO *xg = static_cast<const IO *>(p.x);
+    const IO *dg = static_cast<const IO *>(p.delta);
+    const IO *bg = static_cast<const IO *>(p.Bt);
+    const IO *cg = static_cast<const IO *>(p.Ct);
+    const long long row0 = w.b * p.L + ts;
     const int N = p.N;
-    const bool vec = p.vecBC != 0;
-    const long long nsteps = t1 - t0;
-#pragma unroll 2
-    for (long long s = 0; s < nsteps; ++s) {
-        const long long t = REV ? (t1 - 1 - s) : (t0 + s);
-        const long long row = b * L + t;
-        const long long xi = row * D + d;
-        float xv = 0.0f, dv = 0.0f;
-        if (dvalid) {
-            xv = Io<IO>::ld(xp + xi);
-            dv = Io<IO>::ld(dp + xi);
+    if (p.bulk) {
+        const unsigned xrow = (unsigned)(w.cw * sizeof(IO));
+        const unsigned btile = (unsigned)(nrows * N * sizeof(IO));
+        const unsigned bytes = nrows * 2u * xrow + (MODE == MODE_OUT ? 2u : 1u) * btile;
+        uint64_t *bar = w.bars + slot;
+        if (w.lane == 0) mbar_arrive_expect_tx(bar, bytes);
+        __syncwarp();
+        if (w.lane < nrows) {
+            const long long gi = (row0 + w.lane) * p.D + w.d0;
+            bulk_g2s(xs + w.lane * 32, xg + gi, xrow, bar);
+            bulk_g2s(ds + w.lane * 32, dg + gi, xrow, bar);
         }
-        const float dl = SP ? softplus_mufu(dv) : dv;
-        float Bv[NG];
-        load_states<NG, IO>(bp + row * N, N, vec, Bv);
-        const float u = dl * xv;
-        if constexpr (MODE == MODE_AGG) {
+        if (w.lane == 0) {
+            bulk_g2s(bs, bg + row0 * N, btile, bar);
+            if (MODE == MODE_OUT) bulk_g2s(cs, cg + row0 * N, btile, bar);
+        }
+    } else {
+        // unaligned shapes: plain loads, synchronous
+        for (int r = 0; r < nrows; ++r) {
+            const long long gi = (row0 + r) * p.D + w.d;
+            xs[r * 32 + w.lane] = w.dvalid ? xg[gi] : IO(0.0f);
+            ds[r * 32 + w.lane] = w.dvalid ? dg[gi] : IO(0.0f);
+        }
+        for (int i = w.lane; i < nrows * N; i += 32) {
+            bs[i] = bg[row0 * N + i];
+            if (MODE == MODE_OUT) cs[i] = cg[row0 * N + i];
+        }
+        __syncwarp();
+    }
+}
+
+template <typename IO>
+__device__ __forceinline__ void wait_stage(const S6Params &p, WarpCtx &w, unsigned idx) {
+    if (!p.bulk) return;
+    const int slot = idx % kStages;
+    const unsigned parity = (idx / kStages) & 1u;
+    if (!mbar_wait_bounded(w.bars + slot, parity, kCopyTimeoutNs)) {
+        if (w.lane == 0) record_error(p.ws, SS_ERR_TIMEOUT, 5u, (unsigned)w.b, (unsigned)w.t0);
+        mbar_wait_bounded(w.bars + slot, parity, kCopyTimeoutNs);
+    }
+}
+
+// Output handling of a MODE_OUT sweep.
+enum { OUT_Y = 0,        // store y in the storage type
+       OUT_HALF = 1,     // forward half of a bidirectional output: fp32 to yf
+       OUT_SUM = 2 };    // reverse half: add the fp32 forward half, store y
+
+// 2^(delta * A2) for a pair of states in one PTX block, so both MUFU results
+// land in the two halves of one 64-bit register.
+__device__ __forceinline__ u64 f2_exp2_scaled(u64 dd, u64 a2) {
+    u64 r;
+    asm("{\n .reg .b64 t;\n .reg .f32 lo, hi;\n"
+        " mul.rn.f32x2 t, %1, %2;\n"
+        " mov.b64 {lo, hi}, t;\n"
+        " ex2.approx.ftz.f32 lo, lo;\n"
+        " ex2.approx.ftz.f32 hi, hi;\n"
+        " mov.b64 %0, {lo, hi};\n}"
+        : "=l"(r) : "l"(dd), "l"(a2));
+    return r;
+}
+
+// One timestep of this lane's chains. xv, dv: x and delta of (t, d); brow,
+// crow: Bt and Ct rows of t as fp32; yp: this lane's output element.
+template <int NG, typename IO, bool SP, bool BIDIR, int MODE, int OUT>
+__device__ __forceinline__ void step(float xv, float dv, const float *brow, const float *crow,
+                                     const u64 (&A2)[NG / 2], float Dd, u64 (&h)[NG / 2],
+                                     u64 (&hr)[NG / 2], u64 (&Q)[NG / 2], float &sdel, IO *yp,
+                                     float *yfp, bool store) {
+    const float dl = SP ? softplus_mufu(dv) : dv;
+    const float u = dl * xv;
+    const u64 dd = f2(dl, dl);
+    const u64 uu = f2(u, u);
+    if constexpr (MODE == MODE_AGG) {
 #pragma unroll
-            for (int i = 0; i < NG; ++i) {
-                const float dA = ex2_approx(dl * A2[i]);
-                const float dbx = u * Bv[i];
-                h[i] = fmaf(dA, h[i], dbx);
+        for (int q4 = 0; q4 < NG / 4; ++q4) {
+            const ulonglong2 bq = *reinterpret_cast<const ulonglong2 *>(brow + 4 * q4);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int q2 = 2 * q4 + e;
+                const u64 dA = f2_exp2_scaled(dd, A2[q2]);
+                const u64 dbx = f2mul(uu, e ? bq.y : bq.x);
+                h[q2] = f2fma(dA, h[q2], dbx);
                 if constexpr (BIDIR) {
-                    hr[i] = fmaf(Q[i], dbx, hr[i]);
-                    Q[i] *= dA;
+                    hr[q2] = f2fma(Q[q2], dbx, hr[q2]);
+                    Q[q2] = f2mul(Q[q2], dA);
                 }
             }
-            sdel += dl;
-        } else {
-            float Cv[NG];
-            load_states<NG, IO>(cp + row * N, N, vec, Cv);
-            float acc = 0.0f;
+        }
+        sdel += dl;
+    } else {
+        u64 acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
-            for (int i = 0; i < NG; ++i) {
-                const float dA = ex2_approx(dl * A2[i]);
-                h[i] = fmaf(dA, h[i], u * Bv[i]);
-                acc = fmaf(h[i], Cv[i], acc);
+        for (int q4 = 0; q4 < NG / 4; ++q4) {
+            const ulonglong2 bq = *reinterpret_cast<const ulonglong2 *>(brow + 4 * q4);
+            const ulonglong2 cq = *reinterpret_cast<const ulonglong2 *>(crow + 4 * q4);
+            const u64 dA0 = f2_exp2_scaled(dd, A2[2 * q4]);
+            const u64 dA1 = f2_exp2_scaled(dd, A2[2 * q4 + 1]);
+            h[2 * q4] = f2fma(dA0, h[2 * q4], f2mul(uu, bq.x));
+            h[2 * q4 + 1] = f2fma(dA1, h[2 * q4 + 1], f2mul(uu, bq.y));
+            acc0 = f2fma(h[2 * q4], cq.x, acc0);
+            acc1 = f2fma(h[2 * q4 + 1], cq.y, acc1);
+        }
+        const float accs = (f2lo(acc0) + f2hi(acc0)) + (f2lo(acc1) + f2hi(acc1));
+        const float yv = fmaf(Dd, xv, accs);
+        if (store) {
+            if constexpr (OUT == OUT_Y) store_io(yp, yv);
+            else if constexpr (OUT == OUT_HALF) *yfp = yv;
+            else store_io(yp, yv + *yfp);
+        }
+    }
+}
+
+// One pass of this lane's chains over its timesteps, streamed through the ring.
+// MODE_AGG: from the state in h (zero), accumulate the sub-chunk aggregate.
+// MODE_OUT: from the state in h, write outputs (OUT_* above).
+template <int NG, typename IO, bool SP, bool BIDIR, int MODE, bool REV, int OUT>
+__device__ __forceinline__ void sweep(const S6Params &p, WarpCtx &w, const u64 (&A2)[NG / 2],
+                                      float Dd, u64 (&h)[NG / 2], u64 (&hr)[NG / 2],
+                                      u64 (&Q)[NG / 2], float &sdel, float *yf) {
+    using R = Ring<IO>;
+    const long long len = w.t1 - w.t0;
+    if (len <= 0) return;
+    const int nst = (int)((len + kTS - 1) / kTS);
+    const int N = p.N;
+    const bool conv = (sizeof(IO) == 2) || (N != NG);
+    float *bconv = reinterpret_cast<float *>(w.ring + kStages * R::kSlot);
+    float *cconv = bconv + kTS * 16;
+    const unsigned base = w.issued;
+    const int pre = min(kStages, nst);
+    for (int q = 0; q < pre; ++q) issue_stage<IO, MODE>(p, w, REV ? nst - 1 - q : q, (base + q) % kStages);
+    w.issued += pre;
+    const long long D = p.D;
+    IO *ybase = static_cast<IO *>(p.y) + w.b * p.L * D + w.d;   // y[b, 0, d]
+    float *yfbase = yf ? yf + w.b * p.L * D + w.d : nullptr;
+
+    for (int q = 0; q < nst; ++q) {
+        const unsigned idx = base + q;
+        const int slot = idx % kStages;
+        const int st = REV ? nst - 1 - q : q;
+        wait_stage<IO>(p, w, idx);
+        const unsigned char *sl = w.ring + slot * R::kSlot;
+        const IO *xs = reinterpret_cast<const IO *>(sl) + w.lane;
+        const IO *ds = reinterpret_cast<const IO *>(sl + R::kXBytes) + w.lane;
+        const IO *bs = reinterpret_cast<const IO *>(sl + 2 * R::kXBytes);
+        const IO *cs = reinterpret_cast<const IO *>(sl + 2 * R::kXBytes + R::kBBytes);
+        const long long ts = w.t0 + (long long)st * kTS;
+        const int nrows = (int)min((long long)kTS, w.t1 - ts);
+        if (conv) {
+            // widen / pad the stage's Bt (and Ct) rows to fp32 x 16 states
+            for (int i = w.lane; i < nrows * 16; i += 32) {
+                const int r = i >> 4, n = i & 15;
+                bconv[i] = n < N ? to_f32(bs[r * N + n]) : 0.0f;
+                if (MODE == MODE_OUT) cconv[i] = n < N ? to_f32(cs[r * N + n]) : 0.0f;
             }
-            float yv = fmaf(Dd, xv, acc);
-            if (dvalid) {
-                if (yf == nullptr) {
-                    Io<IO>::st(static_cast<IO *>(p.y) + xi, yv);
-                } else if (!final_out) {
-                    yf[xi] = yv;  // forward half of a bidirectional output
-                } else {
-                    yv += yf[xi];
-                    Io<IO>::st(static_cast<IO *>(p.y) + xi, yv);
-                }
+            __syncwarp();
+        }
+        const float *bf = conv ? bconv : reinterpret_cast<const float *>(bs);
+        const float *cf = conv ? cconv : reinterpret_cast<const float *>(cs);
+        const int bstride = conv ? 16 : NG;
+        IO *yp = ybase + ts * D;
+        float *yfp = yfbase ? yfbase + ts * D : nullptr;
+        if (nrows == kTS) {
+#pragma unroll
+            for (int rr = 0; rr < kTS; ++rr) {
+                const int r = REV ? kTS - 1 - rr : rr;
+                step<NG, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * 32]), to_f32(ds[r * 32]),
+                                                   bf + r * bstride, cf + r * bstride, A2, Dd, h,
+                                                   hr, Q, sdel, yp + r * D,
+                                                   yfp ? yfp + r * D : nullptr, w.dvalid);
             }
+        } else {
+            for (int rr = 0; rr < nrows; ++rr) {
+                const int r = REV ? nrows - 1 - rr : rr;
+                step<NG, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * 32]), to_f32(ds[r * 32]),
+                                                   bf + r * bstride, cf + r * bstride, A2, Dd, h,
+                                                   hr, Q, sdel, yp + r * D,
+                                                   yfp ? yfp + r * D : nullptr, w.dvalid);
+            }
+        }
+        __syncwarp();  // every lane is done with this slot (and the fp32 rows)
+        if (q + kStages < nst) {
+            issue_stage<IO, MODE>(p, w, REV ? nst - 1 - (q + kStages) : q + kStages, slot);
+            w.issued += 1;
         }
     }
 }
 
 // ------------------------------------------------------------------ look-back
 // Warp-parallel walk over the nearest predecessor (FWD) or successor (!FWD)
-// chunks of the same sequence. Lane l examines chunk k -/+ (1 + l + 32*win).
-// Returns the chunk index of the nearest published inclusive state (-1 or K
-// for the sequence boundary, whose state is zero), or -2 on timeout.
+// chunks of the same sequence. Lane l examines chunk k -/+ (1 + l + 32*win)
+// and waits until it holds at least an aggregate. Returns the chunk index of
+// the nearest published inclusive state (-1 or K for the sequence boundary,
+// whose state is zero), or -2 if any wait ran out.
 template <bool FWD>
 __device__ int find_anchor(const S6Params &p, long long seq, int k, unsigned tag, int lane) {
     const uint64_t t0 = globaltimer_ns();
     int win = 0;
     for (;;) {
         const int m = FWD ? k - 1 - (lane + 32 * win) : k + 1 + (lane + 32 * win);
-        bool is_inc;
+        bool is_inc = false, gave_up = false;
         if (FWD ? (m < 0) : (m >= p.K)) {
             is_inc = true;
         } else {
@@ -262,19 +409,15 @@ __device__ int find_anchor(const S6Params &p, long long seq, int k, unsigned tag
                     is_inc = true;
                     break;
                 }
-                if (ld_acquire_u32(fl + FL_AGG) == tag) {
-                    is_inc = false;
-                    break;
-                }
+                if (ld_acquire_u32(fl + FL_AGG) == tag) break;
                 if ((it & 63u) == 63u &&
                     (globaltimer_ns() - t0 > p.timeout_ns || ld_relaxed_u32(&p.ws->error) != 0u)) {
-                    is_inc = false;
-                    it = 0xffffffffu;  // timed out
+                    gave_up = true;
                     break;
                 }
             }
-            // a lane that gave up is reported through the timer check below
         }
+        if (__ballot_sync(kFull, gave_up)) return -2;
         const unsigned incs = __ballot_sync(kFull, is_inc);
         if (incs) {
             const int l = __ffs(incs) - 1;  // nearest lane with an inclusive state
@@ -292,9 +435,12 @@ __global__ void __launch_bounds__(kMaxWT * 32)
 s6_kernel(const S6Params p) {
     constexpr int NSUB = BIDIR ? 3 : 2;  // sub-aggregate fields: P, H (, Hr)
     constexpr int NF = BIDIR ? 5 : 3;    // descriptor fields
-    extern __shared__ __align__(16) float smem[];
-    float *s_sub = smem;                               // [WT][NSUB][32][NG]
-    float *s_car = smem + p.WT * NSUB * 32 * NG;       // [2][32][NG]
+    constexpr int NP = NG / 2;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char *s_ring = smem_raw;                                       // [WT][Ring::kWarp]
+    uint64_t *s_bars = reinterpret_cast<uint64_t *>(s_ring + p.WT * Ring<IO>::kWarp);  // [WT][kStages]
+    float *s_sub = reinterpret_cast<float *>(s_bars + p.WT * kStages);      // [WT][NSUB][32][NG]
+    float *s_car = s_sub + p.WT * NSUB * 32 * NG;                           // [2][32][NG]
 
     const bool chunked = p.K > 1;
     unsigned ticket, tag = 0;
@@ -305,22 +451,39 @@ s6_kernel(const S6Params p) {
     }
     const long long seq = ticket / (unsigned)p.K;
     const int k = (int)(ticket % (unsigned)p.K);
-    const long long b = seq / p.dtiles;
-    const int dt = (int)(seq % p.dtiles);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const long long d = (long long)dt * 32 + lane;
-    const bool dvalid = d < p.D;
+
+    WarpCtx w;
+    w.ring = s_ring + warp * Ring<IO>::kWarp;
+    w.bars = s_bars + warp * kStages;
+    w.issued = 0;
+    w.lane = lane;
+    w.b = seq / p.dtiles;
+    w.d0 = (seq % p.dtiles) * 32;
+    w.d = w.d0 + lane;
+    w.dvalid = w.d < p.D;
+    w.cw = (int)min(32LL, p.D - w.d0);
     const long long tc0 = (long long)k * p.WT * p.Tsub;
-    const long long t0 = min(tc0 + (long long)warp * p.Tsub, p.L);
-    const long long t1 = min(t0 + (long long)p.Tsub, p.L);
+    w.t0 = min(tc0 + (long long)warp * p.Tsub, p.L);
+    w.t1 = min(w.t0 + (long long)p.Tsub, p.L);
+    if (lane == 0 && p.bulk) {
+        for (int s = 0; s < kStages; ++s) mbar_init(w.bars + s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
 
-    float A2[NG];
+    u64 A2[NP];
 #pragma unroll
-    for (int i = 0; i < NG; ++i) A2[i] = (dvalid && i < p.N) ? p.A[d * p.N + i] * kLog2e : 0.0f;
-    const float Dd = (dvalid && p.Dskip) ? p.Dskip[d] : 0.0f;
+    for (int q = 0; q < NP; ++q) {
+        float lo = 0.0f, hi = 0.0f;
+        if (w.dvalid && 2 * q < p.N) lo = p.A[w.d * p.N + 2 * q] * kLog2e;
+        if (w.dvalid && 2 * q + 1 < p.N) hi = p.A[w.d * p.N + 2 * q + 1] * kLog2e;
+        A2[q] = f2(lo, hi);
+    }
+    const float Dd = (w.dvalid && p.Dskip) ? p.Dskip[w.d] : 0.0f;
 
-    float h[NG], hr[NG], Q[NG];
+    u64 h[NP], hr[NP], Q[NP];
     float sdel = 0.0f;
     float cf[NG], cr[NG];
 #pragma unroll
@@ -329,19 +492,24 @@ s6_kernel(const S6Params p) {
     if (chunked || p.WT > 1) {
         // ---- sub-chunk aggregate from a zero state
 #pragma unroll
-        for (int i = 0; i < NG; ++i) {
-            h[i] = 0.0f;
-            hr[i] = 0.0f;
-            Q[i] = 1.0f;
+        for (int q = 0; q < NP; ++q) {
+            h[q] = 0ull;
+            hr[q] = 0ull;
+            Q[q] = f2(1.0f, 1.0f);
         }
-        sweep<NG, IO, SP, BIDIR, MODE_AGG, false>(p, b, d, dvalid, t0, t1, A2, Dd, h, hr, Q, sdel,
-                                                 nullptr, false);
-        float *mine = s_sub + ((warp * NSUB) * 32 + lane) * NG;
+        sweep<NG, IO, SP, BIDIR, MODE_AGG, false, OUT_Y>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
+        // s_sub[((w*NSUB + field)*NG + i)*32 + lane]: lane-fastest, conflict-free
+        float *mine = s_sub + warp * NSUB * NG * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < NG; ++i) {
-            mine[i] = ex2_approx(A2[i] * sdel);  // prod of dA over the sub-chunk
-            mine[32 * NG + i] = h[i];
-            if constexpr (BIDIR) mine[2 * 32 * NG + i] = hr[i];
+        for (int q = 0; q < NP; ++q) {
+            mine[(2 * q) * 32] = ex2_approx(f2lo(A2[q]) * sdel);  // prod of dA over the sub-chunk
+            mine[(2 * q + 1) * 32] = ex2_approx(f2hi(A2[q]) * sdel);
+            mine[(NG + 2 * q) * 32] = f2lo(h[q]);
+            mine[(NG + 2 * q + 1) * 32] = f2hi(h[q]);
+            if constexpr (BIDIR) {
+                mine[(2 * NG + 2 * q) * 32] = f2lo(hr[q]);
+                mine[(2 * NG + 2 * q + 1) * 32] = f2hi(hr[q]);
+            }
         }
         __syncthreads();
 
@@ -355,19 +523,20 @@ s6_kernel(const S6Params p) {
                     Hc[i] = 0.0f;
                     Hrc[i] = 0.0f;
                 }
-                for (int w = 0; w < p.WT; ++w) {
-                    const float *s = s_sub + ((w * NSUB) * 32 + lane) * NG;
+                for (int v = 0; v < p.WT; ++v) {
+                    const float *s = s_sub + v * NSUB * NG * 32 + lane;
 #pragma unroll
                     for (int i = 0; i < NG; ++i) {
-                        Pc[i] *= s[i];
-                        Hc[i] = fmaf(s[i], Hc[i], s[32 * NG + i]);
+                        Pc[i] *= s[i * 32];
+                        Hc[i] = fmaf(s[i * 32], Hc[i], s[(NG + i) * 32]);
                     }
                 }
                 if constexpr (BIDIR) {
-                    for (int w = p.WT - 1; w >= 0; --w) {
-                        const float *s = s_sub + ((w * NSUB) * 32 + lane) * NG;
+                    for (int v = p.WT - 1; v >= 0; --v) {
+                        const float *s = s_sub + v * NSUB * NG * 32 + lane;
 #pragma unroll
-                        for (int i = 0; i < NG; ++i) Hrc[i] = fmaf(s[i], Hrc[i], s[2 * 32 * NG + i]);
+                        for (int i = 0; i < NG; ++i)
+                            Hrc[i] = fmaf(s[i * 32], Hrc[i], s[(2 * NG + i) * 32]);
                     }
                 }
                 const long long unit = seq * p.K + k;
@@ -421,8 +590,8 @@ s6_kernel(const S6Params p) {
             }
 #pragma unroll
             for (int i = 0; i < NG; ++i) {
-                s_car[lane * NG + i] = cf[i];
-                s_car[(32 + lane) * NG + i] = cr[i];
+                s_car[i * 32 + lane] = cf[i];
+                s_car[(NG + i) * 32 + lane] = cr[i];
             }
         }
         __syncthreads();
@@ -431,35 +600,34 @@ s6_kernel(const S6Params p) {
         // (forward) or later (reverse) sub-chunks of the CTA, in order
 #pragma unroll
         for (int i = 0; i < NG; ++i) {
-            cf[i] = s_car[lane * NG + i];
-            cr[i] = s_car[(32 + lane) * NG + i];
+            cf[i] = s_car[i * 32 + lane];
+            cr[i] = s_car[(NG + i) * 32 + lane];
         }
-        for (int w = 0; w < warp; ++w) {
-            const float *s = s_sub + ((w * NSUB) * 32 + lane) * NG;
+        for (int v = 0; v < warp; ++v) {
+            const float *s = s_sub + v * NSUB * NG * 32 + lane;
 #pragma unroll
-            for (int i = 0; i < NG; ++i) cf[i] = fmaf(s[i], cf[i], s[32 * NG + i]);
+            for (int i = 0; i < NG; ++i) cf[i] = fmaf(s[i * 32], cf[i], s[(NG + i) * 32]);
         }
         if constexpr (BIDIR) {
-            for (int w = p.WT - 1; w > warp; --w) {
-                const float *s = s_sub + ((w * NSUB) * 32 + lane) * NG;
+            for (int v = p.WT - 1; v > warp; --v) {
+                const float *s = s_sub + v * NSUB * NG * 32 + lane;
 #pragma unroll
-                for (int i = 0; i < NG; ++i) cr[i] = fmaf(s[i], cr[i], s[2 * 32 * NG + i]);
+                for (int i = 0; i < NG; ++i) cr[i] = fmaf(s[i * 32], cr[i], s[(2 * NG + i) * 32]);
             }
         }
     }
 
     // ---- outputs: forward sweep from the carry (and the reverse sweep)
 #pragma unroll
-    for (int i = 0; i < NG; ++i) h[i] = cf[i];
-    float *yf = nullptr;
-    if constexpr (BIDIR) yf = p.yscratch ? p.yscratch : static_cast<float *>(p.y);
-    sweep<NG, IO, SP, BIDIR, MODE_OUT, false>(p, b, d, dvalid, t0, t1, A2, Dd, h, hr, Q, sdel, yf,
-                                             false);
+    for (int q = 0; q < NP; ++q) h[q] = f2(cf[2 * q], cf[2 * q + 1]);
     if constexpr (BIDIR) {
+        float *yf = p.yscratch ? p.yscratch : static_cast<float *>(p.y);
+        sweep<NG, IO, SP, BIDIR, MODE_OUT, false, OUT_HALF>(p, w, A2, Dd, h, hr, Q, sdel, yf);
 #pragma unroll
-        for (int i = 0; i < NG; ++i) h[i] = cr[i];
-        sweep<NG, IO, SP, BIDIR, MODE_OUT, true>(p, b, d, dvalid, t0, t1, A2, Dd, h, hr, Q, sdel, yf,
-                                                true);
+        for (int q = 0; q < NP; ++q) h[q] = f2(cr[2 * q], cr[2 * q + 1]);
+        sweep<NG, IO, SP, BIDIR, MODE_OUT, true, OUT_SUM>(p, w, A2, Dd, h, hr, Q, sdel, yf);
+    } else {
+        sweep<NG, IO, SP, BIDIR, MODE_OUT, false, OUT_Y>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
     }
 
     if (chunked) finish_launch(p.ws, tag);
@@ -469,7 +637,7 @@ s6_kernel(const S6Params p) {
 struct Plan {
     int NG, WT, K, Tsub, dtiles;
     long long seqs;
-    size_t desc_bytes, flag_bytes, payload_bytes, scratch_bytes, total;
+    size_t flag_bytes, payload_bytes, scratch_bytes, desc_bytes, total;
     size_t smem;
 };
 
@@ -492,15 +660,15 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     const long long target_warps = sms * 16;
     long long S = (target_warps + pl.seqs - 1) / std::max<long long>(pl.seqs, 1);
     S = std::max<long long>(1, std::min<long long>(S, (L + 31) / 32));
-    int WT = (int)std::min<long long>(S, kMaxWT);
+    int WT = (int)std::min<long long>(S, kDefaultWT);
     long long K = (S + WT - 1) / WT;
     long long Tsub = (L + K * WT - 1) / (K * WT);
-    Tsub = (Tsub + 3) / 4 * 4;
+    Tsub = (Tsub + kTS - 1) / kTS * kTS;
     if (const char *e = std::getenv("SS_S6_WT_TSUB")) {  // tuning override "WT,Tsub"
-        int w = 0, t = 0;
-        if (std::sscanf(e, "%d,%d", &w, &t) == 2 && w >= 1 && w <= kMaxWT && t >= 1) {
-            WT = w;
-            Tsub = t;
+        int wv = 0, tv = 0;
+        if (std::sscanf(e, "%d,%d", &wv, &tv) == 2 && wv >= 1 && wv <= kMaxWT && tv >= 1) {
+            WT = wv;
+            Tsub = tv;
         }
     }
     K = std::max<long long>(1, (L + (long long)WT * Tsub - 1) / ((long long)WT * Tsub));
@@ -518,7 +686,9 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     pl.desc_bytes = pl.flag_bytes + pl.payload_bytes;
     pl.total = 0;
     if (pl.K > 1 || pl.scratch_bytes) pl.total = kWsHeaderBytes + pl.desc_bytes + pl.scratch_bytes;
-    pl.smem = (size_t)(pl.WT * NSUB + 2) * 32 * pl.NG * sizeof(float);
+    const size_t ring = io_bf16 ? Ring<__nv_bfloat16>::kWarp : Ring<float>::kWarp;
+    pl.smem = (size_t)pl.WT * (ring + kStages * sizeof(uint64_t)) +
+              (size_t)(pl.WT * NSUB + 2) * 32 * pl.NG * sizeof(float);
     return pl;
 }
 
@@ -590,15 +760,17 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
     prm.WT = pl.WT;
     prm.Tsub = pl.Tsub;
     const size_t es = a.io_bf16 ? 2 : 4;
-    const uintptr_t al = reinterpret_cast<uintptr_t>(a.Bt) | reinterpret_cast<uintptr_t>(a.Ct);
-    prm.vecBC = (a.N == pl.NG) && ((a.N * es) % 16 == 0) && (al % 16 == 0);
+    const uintptr_t al = reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.delta) |
+                         reinterpret_cast<uintptr_t>(a.Bt) | reinterpret_cast<uintptr_t>(a.Ct);
+    prm.bulk = ((a.D * es) % 16 == 0) && ((a.N * es) % 16 == 0) && (al % 16 == 0);
     prm.timeout_ns = timeout_ns;
     prm.skip_unit = skip_unit;
     char *ws = static_cast<char *>(workspace);
     prm.ws = reinterpret_cast<WsHeader *>(ws);
     prm.flags = pl.K > 1 ? reinterpret_cast<unsigned *>(ws + kWsHeaderBytes) : nullptr;
     prm.payload = pl.K > 1 ? reinterpret_cast<float *>(ws + kWsHeaderBytes + pl.flag_bytes) : nullptr;
-    prm.yscratch = pl.scratch_bytes ? reinterpret_cast<float *>(ws + kWsHeaderBytes + pl.desc_bytes) : nullptr;
+    prm.yscratch =
+        pl.scratch_bytes ? reinterpret_cast<float *>(ws + kWsHeaderBytes + pl.desc_bytes) : nullptr;
     const bool sp = a.softplus != 0, bd = a.bidir != 0;
     return a.io_bf16 ? launch_io<__nv_bfloat16>(prm, pl, sp, bd, stream)
                      : launch_io<float>(prm, pl, sp, bd, stream);

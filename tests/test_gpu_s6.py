@@ -86,7 +86,7 @@ def test_small_shapes(torch, ss, shape, io, softplus, bidir):
 
 
 @pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
-@pytest.mark.parametrize("wt,tsub", [(1, 1), (1, 7), (2, 8), (3, 5), (8, 4), (4, 33), (8, 64)])
+@pytest.mark.parametrize("wt,tsub", [(1, 3), (1, 7), (2, 8), (3, 5), (8, 4), (4, 33), (8, 64)])
 def test_chunk_splits(torch, ss, plan_override, wt, tsub, bidir):
     """Forces many chunks and sub-chunks so the look-back, the look-forward
     and the in-CTA folds run across ragged boundaries."""
@@ -94,6 +94,24 @@ def test_chunk_splits(torch, ss, plan_override, wt, tsub, bidir):
     inp = small(2, 777, 70, 16, seed=wt * 100 + tsub)
     y = gpu_run(ss, torch, inp, False, bidir)
     assert rel_err(y, oracle_run(inp, False, bidir)) <= TOL["f32"]
+
+
+def test_forward_with_one_step_chunks(torch, ss, plan_override):
+    """777 chunks of one timestep each: the look-back walks several windows."""
+    plan_override(1, 1)
+    inp = small(2, 777, 70, 16, seed=101)
+    y = gpu_run(ss, torch, inp, False, False)
+    assert rel_err(y, oracle_run(inp, False, False)) <= TOL["f32"]
+
+
+def test_bidir_refuses_more_chunks_than_fit(torch, ss, plan_override):
+    """Every chunk of a bidirectional sequence must be resident at once; a
+    plan that cannot be is refused up front instead of risking a stall."""
+    plan_override(1, 1)
+    inp = small(1, 20000, 32, 16, seed=3)
+    with pytest.raises(ss.SSError) as e:
+        gpu_run(ss, torch, inp, False, True)
+    assert e.value.status == ss.SS_ERR_UNSUPPORTED
 
 
 def test_chunked_bf16_softplus(torch, ss, plan_override):
