@@ -6,41 +6,56 @@
 // walk and several items per thread scanned in registers. This is a new
 // sm_103a kernel built on that idea:
 //
-//  * one CTA per 4096-element tile; tile ids come from a ticket counter in
-//    CTA start order, so every lower tile is running or done;
-//  * the tile's a and b are staged into shared memory by two bulk async
-//    copies (cp.async.bulk) completing on an mbarrier;
+//  * a persistent grid (as many CTAs as fit) takes 4096-element tiles from a
+//    ticket counter in start order, so every lower tile is running or done;
+//  * each CTA owns a ring of kBufs tile buffers in shared memory, filled by
+//    two bulk async copies (cp.async.bulk) per tile on an mbarrier, 8 compute
+//    warps and one control warp. Per step the compute warps scan the next
+//    tile and publish its aggregate while the control warp looks back for the
+//    current tile; the compute warps then fix up and store the current tile
+//    and refill its buffer with the tile kBufs ahead, and the look-back
+//    overlaps the scan;
 //  * each warp owns 512 consecutive elements as four 128-element stripes;
 //    a lane scans its four-element slice of each stripe in registers, then
 //    four interleaved warp-shuffle scans and a fold over the 8 warps give
 //    the tile aggregate;
-//  * the aggregate is published as two tagged 64-bit words; warp 0 walks
-//    back 32 predecessors at a time to the nearest tile that has published
-//    its inclusive state, and lane 0 applies the aggregates after it to that
-//    state one by one, in sequence order;
+//  * the aggregate is published as two tagged 64-bit words; the control warp
+//    walks back 32 predecessors at a time to the nearest tile that has
+//    published its inclusive state, and lane 0 applies the aggregates after
+//    it to that state one by one, in sequence order;
 //  * the tile's inclusive state is published, and each lane re-sweeps its
 //    elements from shared memory starting at its carry-in, storing h with
-//    coalesced 128-bit stores.
+//    coalesced 128-bit streaming stores.
 //
 // Determinism: a tile publishes I_k = a_k * e_k + b_k (one fma) where e_k is
 // the state entering the tile. Applying predecessor aggregates to a state
 // with the same fma in sequence order reproduces I_{k-1} bit for bit, no
 // matter which earlier tile the walk started from, so e_k == I_{k-1} always
 // and every output is independent of scheduling.
+//
+// Progress: a CTA holds at most kBufs + 1 tickets (current and the ones after it),
+// scanned and published in ticket order. The lowest unfinished tile is
+// always some CTA's current tile and every tile below it is finished, so its
+// look-back completes.
+#include <algorithm>
+
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
 namespace ss {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                // compute threads (8 warps)
 constexpr int kWarps = kThreads / 32;
+constexpr int kCtaThreads = kThreads + 32;  // plus one control warp
 constexpr int kItems = 16;                 // elements per thread
 constexpr int kTile = kThreads * kItems;   // 4096 elements per tile
 constexpr int kStripes = kItems / 4;       // float4 slices per thread
 constexpr int kWarpElems = 32 * kItems;    // 512 elements per warp
 constexpr int kMaxWindows = 8;             // look-back holds up to 256 predecessors
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kBufs = 2;                                     // tile buffers per CTA
+constexpr size_t kDynSmem = 2 * kBufs * kTile * sizeof(float);  // a and b per buffer
 constexpr unsigned long long kCopyTimeoutNs = 2000000000ull;  // bulk-copy completion bound
 
 struct TileDesc {
@@ -54,6 +69,11 @@ static_assert(sizeof(TileDesc) == 32, "descriptor is 32 bytes");
 struct Pair {
     float a, b;
 };
+
+// Barrier among the 8 compute warps only (the control warp does not take part).
+__device__ __forceinline__ void compute_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
 
 // p then q: x -> q.a * (p.a * x + p.b) + q.b  ==  (p.a*q.a, q.a*p.b + q.b).
 __device__ __forceinline__ Pair compose(Pair p, Pair q) {
@@ -74,80 +94,57 @@ struct AffineParams {
     int vec_out;   // h is 16-byte aligned
 };
 
-// Polls tile t's descriptor until it holds at least an aggregate.
-// kind: 2 = inclusive state available (val), 1 = aggregate (agg), 0 = timed out.
-__device__ __forceinline__ int poll_desc(const TileDesc *d, unsigned tag, WsHeader *ws,
-                                         unsigned long long timeout_ns, float &val, Pair &agg) {
-    uint64_t t0 = 0;
-    for (unsigned it = 0;; ++it) {
-        const unsigned long long inc = ld_relaxed_u64(&d->inc);
-        if (tag_of(inc) == tag) {
-            val = val_of(inc);
-            return 2;
+// Per-tile results of the in-tile scan that the fix-up needs later.
+struct TileScan {
+    Pair ex[kStripes];    // exclusive prefix of this lane within stripe j
+    Pair qpre[kStripes];  // composition of the warp's earlier stripes
+    Pair rpre;            // composition of the CTA's earlier warps
+    Pair tagg;            // tile aggregate (thread 0 only)
+};
+
+// Starts staging tile `tile` into (sa, sb): two bulk copies on `bar` for a
+// full tile of aligned inputs, else plain loads with identity padding
+// (completed by the barrier that precedes the tile's scan).
+__device__ __forceinline__ void stage_tile(const AffineParams &p, unsigned tile, float *sa,
+                                           float *sb, uint64_t *bar) {
+    const long long base = (long long)tile * kTile;
+    const long long rem = p.n - base;
+    if (p.bulk_ok && rem >= kTile) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(bar, 2u * kTile * sizeof(float));
+            bulk_g2s(sa, p.a + base, kTile * sizeof(float), bar);
+            bulk_g2s(sb, p.b + base, kTile * sizeof(float), bar);
         }
-        const unsigned long long wa = ld_relaxed_u64(&d->agg_a);
-        const unsigned long long wb = ld_relaxed_u64(&d->agg_b);
-        if (tag_of(wa) == tag && tag_of(wb) == tag) {
-            agg = {val_of(wa), val_of(wb)};
-            return 1;
-        }
-        if (it == 0) {
-            t0 = globaltimer_ns();
-        } else if ((it & 63u) == 0u) {
-            if (globaltimer_ns() - t0 > timeout_ns || ld_relaxed_u32(&ws->error) != 0u)
-                return 0;
+    } else {
+        const int valid = rem >= kTile ? kTile : (int)rem;
+        for (int i = threadIdx.x; i < kTile; i += kThreads) {
+            const bool in = i < valid;
+            sa[i] = in ? p.a[base + i] : 1.0f;
+            sb[i] = in ? p.b[base + i] : 0.0f;
         }
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
-affine_scan_kernel(const AffineParams p) {
-    __shared__ __align__(128) float s_a[kTile];
-    __shared__ __align__(128) float s_b[kTile];
-    __shared__ __align__(8) uint64_t s_bar;
-    __shared__ Pair s_warp[kWarps];
-    __shared__ Pair s_walk[kMaxWindows * 32];
-    __shared__ float s_carry;
-
-    unsigned tile, tag;
-    take_ticket(p.ws, tile, tag);
-
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    const long long base = (long long)tile * kTile;
-    const long long rem = p.n - base;
-    const int valid = rem >= kTile ? kTile : (int)rem;
-
-    // ---- load: stage a and b of the tile in shared memory
-    if (p.bulk_ok && valid == kTile) {
-        if (tid == 0) {
-            mbar_init(&s_bar, 1);
-            fence_mbar_init();
-        }
-        __syncthreads();
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&s_bar, 2u * kTile * sizeof(float));
-            bulk_g2s(s_a, p.a + base, kTile * sizeof(float), &s_bar);
-            bulk_g2s(s_b, p.b + base, kTile * sizeof(float), &s_bar);
-        }
-        if (!mbar_wait_bounded(&s_bar, 0, kCopyTimeoutNs)) {
+// Waits for tile `tile`'s data (load number `use` of buffer `bar`), scans it
+// and publishes its aggregate. The compute warps call it; the tile aggregate is
+// left in *s_tagg for the control warp.
+__device__ __forceinline__ void scan_tile(const AffineParams &p, unsigned tile, unsigned tag,
+                                          const float *s_a, const float *s_b, uint64_t *bar,
+                                          unsigned use, Pair *s_warp, Pair *s_tagg, TileScan &r) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long rem = p.n - (long long)tile * kTile;
+    if (p.bulk_ok && rem >= kTile) {
+        const unsigned parity = use & 1u;
+        if (!mbar_wait_bounded(bar, parity, kCopyTimeoutNs)) {
             record_error(p.ws, SS_ERR_TIMEOUT, 1u, tile, 0u);
             // wait once more so no copy is still writing when the CTA leaves
-            mbar_wait_bounded(&s_bar, 0, kCopyTimeoutNs);
+            mbar_wait_bounded(bar, parity, kCopyTimeoutNs);
         }
-    } else {
-        // ragged last tile or unaligned inputs: plain loads, identity padding
-        for (int i = tid; i < kTile; i += kThreads) {
-            const bool in = i < valid;
-            s_a[i] = in ? p.a[base + i] : 1.0f;
-            s_b[i] = in ? p.b[base + i] : 0.0f;
-        }
-        __syncthreads();
     }
+    compute_sync();  // plain-loaded tiles: every thread's writes are visible
 
-    // ---- thread scan: aggregate of each four-element slice
-    Pair st[kStripes];
+    // thread scan: aggregate of each four-element slice
+    Pair inc[kStripes];
 #pragma unroll
     for (int j = 0; j < kStripes; ++j) {
         const int off = warp * kWarpElems + j * 128 + lane * 4;
@@ -157,13 +154,9 @@ affine_scan_kernel(const AffineParams p) {
         q = compose(q, {va.y, vb.y});
         q = compose(q, {va.z, vb.z});
         q = compose(q, {va.w, vb.w});
-        st[j] = q;
+        inc[j] = q;
     }
-
-    // ---- warp scans over lanes, one per stripe (left operand = earlier lane)
-    Pair inc[kStripes];
-#pragma unroll
-    for (int j = 0; j < kStripes; ++j) inc[j] = st[j];
+    // warp scans over lanes, one per stripe (left operand = earlier lane)
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
 #pragma unroll
@@ -173,109 +166,155 @@ affine_scan_kernel(const AffineParams p) {
             if (lane >= off) inc[j] = compose({pa, pb}, inc[j]);
         }
     }
-    Pair ex[kStripes];    // exclusive prefix of this lane within stripe j
-    Pair qpre[kStripes];  // composition of the warp's earlier stripes
     Pair wagg = {1.0f, 0.0f};
 #pragma unroll
     for (int j = 0; j < kStripes; ++j) {
         const float ea = __shfl_up_sync(kFull, inc[j].a, 1);
         const float eb = __shfl_up_sync(kFull, inc[j].b, 1);
-        ex[j] = lane == 0 ? Pair{1.0f, 0.0f} : Pair{ea, eb};
+        r.ex[j] = lane == 0 ? Pair{1.0f, 0.0f} : Pair{ea, eb};
         const Pair tot = {__shfl_sync(kFull, inc[j].a, 31), __shfl_sync(kFull, inc[j].b, 31)};
-        qpre[j] = wagg;
+        r.qpre[j] = wagg;
         wagg = compose(wagg, tot);
     }
     if (lane == 0) s_warp[warp] = wagg;
-    __syncthreads();
-
-    // ---- block: this warp's exclusive prefix and the tile aggregate
-    Pair rpre = {1.0f, 0.0f};
-    for (int w = 0; w < warp; ++w) rpre = compose(rpre, s_warp[w]);
-
-    Pair tagg = {1.0f, 0.0f};
-    const bool publish = (long long)tile != p.skip_unit;
+    compute_sync();
+    r.rpre = {1.0f, 0.0f};
+    for (int w = 0; w < warp; ++w) r.rpre = compose(r.rpre, s_warp[w]);
+    r.tagg = {1.0f, 0.0f};
     if (tid == 0) {
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) tagg = compose(tagg, s_warp[w]);
-        TileDesc *d = p.desc + tile;
-        if (publish) {
-            st_relaxed_u64(&d->agg_a, pack_tagged(tag, tagg.a));
-            st_relaxed_u64(&d->agg_b, pack_tagged(tag, tagg.b));
-            if (tile == 0) st_relaxed_u64(&d->inc, pack_tagged(tag, tagg.b));
+        for (int w = 0; w < kWarps; ++w) r.tagg = compose(r.tagg, s_warp[w]);
+        *s_tagg = r.tagg;
+        if ((long long)tile != p.skip_unit) {
+            TileDesc *d = p.desc + tile;
+            st_relaxed_u64(&d->agg_a, pack_tagged(tag, r.tagg.a));
+            st_relaxed_u64(&d->agg_b, pack_tagged(tag, r.tagg.b));
+            if (tile == 0) st_relaxed_u64(&d->inc, pack_tagged(tag, r.tagg.b));
         }
     }
+    compute_sync();  // s_warp is free for the next tile
+}
 
-    // ---- look-back (warp 0)
-    if (warp == 0) {
-        float e = 0.0f;
-        if (tile > 0) {
-            int win = 0;
-            int anchor_lane = -1;
-            float anchor = 0.0f;
-            bool timed_out = false;
-            const uint64_t walk_t0 = globaltimer_ns();
-            for (;;) {
-                const long long t = (long long)tile - 32LL * (win + 1) + lane;
-                int kind;
-                float v = 0.0f;
-                Pair g = {1.0f, 0.0f};
-                if (t < 0) {
-                    kind = 2;  // the state before tile 0 is h[-1] = 0
-                } else {
-                    kind = poll_desc(p.desc + t, tag, p.ws, p.timeout_ns, v, g);
+// Control warp: the state entering `tile` (nearest published inclusive state,
+// then the aggregates after it applied in sequence order); publishes the
+// tile's inclusive state and leaves the carry in *s_carry.
+// Windows of 32 predecessors are polled nearest first (lane l holds tile
+// tile - 32(w+1) + l); the walk stops at the first window holding an
+// inclusive state, after every tile above it has shown its aggregate.
+__device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, unsigned tag,
+                                          const Pair &tagg, Pair *s_walk, float *s_carry) {
+    const int lane = threadIdx.x & 31;
+    float e = 0.0f;
+    if (tile > 0) {
+        int win = 0;
+        int anchor_lane = -1;
+        float anchor = 0.0f;
+        bool timed_out = false;
+        const uint64_t walk_t0 = globaltimer_ns();
+        for (;;) {
+            const long long t = (long long)tile - 32LL * (win + 1) + lane;
+            int kind = 2;  // before tile 0: the state h[-1] = 0 counts as inclusive
+            float v = 0.0f;
+            Pair g = {1.0f, 0.0f};
+            if (t >= 0) {
+                const TileDesc *d = p.desc + t;
+                kind = 0;
+                for (unsigned it = 0;; ++it) {
+                    const unsigned long long wi = ld_relaxed_u64(&d->inc);
+                    if (tag_of(wi) == tag) {
+                        v = val_of(wi);
+                        kind = 2;
+                        break;
+                    }
+                    const unsigned long long wa = ld_relaxed_u64(&d->agg_a);
+                    const unsigned long long wb = ld_relaxed_u64(&d->agg_b);
+                    if (tag_of(wa) == tag && tag_of(wb) == tag) {
+                        g = {val_of(wa), val_of(wb)};
+                        kind = 1;
+                        break;
+                    }
+                    if ((it & 63u) == 63u &&
+                        (globaltimer_ns() - walk_t0 > p.timeout_ns || ld_relaxed_u32(&p.ws->error) != 0u))
+                        break;  // kind stays 0: gave up
                 }
-                s_walk[win * 32 + lane] = g;
-                const unsigned bad = __ballot_sync(kFull, kind == 0);
-                if (bad) {
-                    timed_out = true;
-                    break;
-                }
-                const unsigned incs = __ballot_sync(kFull, kind == 2);
-                if (incs) {
-                    anchor_lane = 31 - __clz(incs);
-                    anchor = __shfl_sync(kFull, v, anchor_lane);
-                    break;
-                }
-                if (win + 1 < kMaxWindows) {
-                    ++win;
-                } else if (globaltimer_ns() - walk_t0 > p.timeout_ns ||
-                           ld_relaxed_u32(&p.ws->error) != 0u) {
-                    timed_out = true;  // oldest window never showed an inclusive state
-                    break;
-                }  // else poll the oldest window again
             }
-            __syncwarp();
-            if (timed_out) {
-                if (lane == 0) record_error(p.ws, SS_ERR_TIMEOUT, 2u, tile, (unsigned)win);
-            } else if (lane == 0) {
-                // anchor state, then the aggregates after it, oldest first
-                float s = anchor;
-                for (int i = win * 32 + anchor_lane + 1; i < win * 32 + 32; ++i) s = apply(s_walk[i], s);
-                for (int w = win - 1; w >= 0; --w) {
-                    const Pair *q = s_walk + w * 32;
-#pragma unroll 8
-                    for (int i = 0; i < 32; ++i) s = apply(q[i], s);
-                }
-                e = s;
+            s_walk[win * 32 + lane] = g;
+            if (__ballot_sync(kFull, kind == 0)) {
+                timed_out = true;
+                break;
             }
+            const unsigned incs = __ballot_sync(kFull, kind == 2);
+            if (incs) {
+                anchor_lane = 31 - __clz(incs);
+                anchor = __shfl_sync(kFull, v, anchor_lane);
+                break;
+            }
+            if (win + 1 < kMaxWindows) {
+                ++win;
+            } else if (globaltimer_ns() - walk_t0 > p.timeout_ns ||
+                       ld_relaxed_u32(&p.ws->error) != 0u) {
+                timed_out = true;  // oldest window never showed an inclusive state
+                break;
+            }  // else poll the oldest window again
         }
-        if (lane == 0) {
-            s_carry = e;
-            if (tile > 0 && publish)
-                st_relaxed_u64(&p.desc[tile].inc, pack_tagged(tag, apply(tagg, e)));
+        __syncwarp();
+        if (timed_out) {
+            if (lane == 0) record_error(p.ws, SS_ERR_TIMEOUT, 2u, tile, (unsigned)win);
+        } else if (lane == 0) {
+            // anchor state, then the aggregates after it, oldest first; one
+            // fma per aggregate with operands fetched ahead
+            float s = anchor;
+            {
+                const float4 *q = reinterpret_cast<const float4 *>(s_walk + win * 32);
+                float4 v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = q[i];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (2 * i > anchor_lane) s = fmaf(v[i].x, s, v[i].y);
+                    if (2 * i + 1 > anchor_lane) s = fmaf(v[i].z, s, v[i].w);
+                }
+            }
+            for (int w = win - 1; w >= 0; --w) {
+                const float4 *q = reinterpret_cast<const float4 *>(s_walk + w * 32);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float4 v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = q[4 * c + i];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        s = fmaf(v[i].x, s, v[i].y);
+                        s = fmaf(v[i].z, s, v[i].w);
+                    }
+                }
+            }
+            e = s;
         }
     }
-    __syncthreads();
+    if (lane == 0) {
+        *s_carry = e;
+        if (tile > 0 && (long long)tile != p.skip_unit)
+            st_relaxed_u64(&p.desc[tile].inc, pack_tagged(tag, apply(tagg, e)));
+    }
+    __syncwarp();
+}
 
-    // ---- fix-up: re-sweep each slice from its carry-in, store h
-    const float ew = apply(rpre, s_carry);
+// Re-sweeps each lane's slices of `tile` from the carry-in and stores h.
+__device__ __forceinline__ void fix_up(const AffineParams &p, unsigned tile, const float *s_a,
+                                       const float *s_b, const TileScan &r, float carry) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long base = (long long)tile * kTile;
+    const long long rem = p.n - base;
+    const int valid = rem >= kTile ? kTile : (int)rem;
+    const float ew = apply(r.rpre, carry);
 #pragma unroll
     for (int j = 0; j < kStripes; ++j) {
         const int off = warp * kWarpElems + j * 128 + lane * 4;
         const float4 va = *reinterpret_cast<const float4 *>(&s_a[off]);
         const float4 vb = *reinterpret_cast<const float4 *>(&s_b[off]);
         float4 o;
-        float s = apply(ex[j], apply(qpre[j], ew));
+        float s = apply(r.ex[j], apply(r.qpre[j], ew));
         o.x = s = fmaf(va.x, s, vb.x);
         o.y = s = fmaf(va.y, s, vb.y);
         o.z = s = fmaf(va.z, s, vb.z);
@@ -290,8 +329,115 @@ affine_scan_kernel(const AffineParams p) {
             if (off + 3 < valid) p.h[g + 3] = o.w;
         }
     }
+}
 
-    finish_launch(p.ws, tag);
+// Shared state of one CTA of the affine-scan kernel.
+struct AffineShared {
+    uint64_t bar[kBufs];       // one mbarrier per tile buffer
+    Pair warp_agg[kWarps];     // per-warp aggregates of the tile being scanned
+    Pair tagg[2];              // tile aggregates handed to the control warp
+    unsigned tick[kBufs];      // tickets of the tiles staged or about to be
+    unsigned tag;              // this launch's descriptor tag
+    float carry;               // state entering the current tile
+};
+
+// Control warp: per step, take the ticket of tile q + kBufs, look back for
+// tile q, then meet the compute warps at the step's two barriers.
+__device__ __forceinline__ void control_loop(const AffineParams &p, AffineShared &sh, Pair *s_walk,
+                                             unsigned num_tiles) {
+    const int lane = threadIdx.x & 31;
+    const unsigned tag = sh.tag;
+    unsigned cur = sh.tick[0], nxt = sh.tick[1];
+    __syncthreads();  // the compute warps' scan of tile 0 (its aggregate) is done
+    for (unsigned q = 0; cur < num_tiles; ++q) {
+        // ticket first: its round trip overlaps the look-back's polls
+        unsigned t = 0;
+        if (lane == 0) t = atomicAdd(&p.ws->ticket, 1u);
+        look_back(p, cur, tag, sh.tagg[q & 1], s_walk, &sh.carry);
+        if (lane == 0) sh.tick[q % kBufs] = t;
+        __syncthreads();  // carry and ticket are published
+        __syncthreads();  // tile q is stored, its buffer restaged
+        cur = nxt;
+        nxt = sh.tick[(q + 2) % kBufs];
+    }
+}
+
+// Compute warps: per step, scan tile q + 1 (publishing its aggregate), then
+// fix up and store tile q and restage its buffer. Two steps per loop trip so
+// the two scan results swap roles without indexing (tile q's results are in
+// rc for even q, in rn for odd q).
+__device__ __forceinline__ void compute_loop(const AffineParams &p, AffineShared &sh, float *s_dyn,
+                                             unsigned num_tiles) {
+    const unsigned tag = sh.tag;
+    auto abuf = [&](unsigned q) { return s_dyn + (q % kBufs) * (2 * kTile); };
+    unsigned cur = sh.tick[0], nxt = sh.tick[1];
+    for (int i = 0; i < kBufs; ++i) {
+        const unsigned t = sh.tick[i];
+        if (t < num_tiles) stage_tile(p, t, abuf(i), abuf(i) + kTile, &sh.bar[i]);
+    }
+    TileScan rc, rn;
+    if (cur < num_tiles)
+        scan_tile(p, cur, tag, abuf(0), abuf(0) + kTile, &sh.bar[0], 0u, sh.warp_agg, &sh.tagg[0], rc);
+    __syncthreads();  // tile 0's aggregate is visible to the control warp
+    for (unsigned q = 0; cur < num_tiles; q += 2) {
+        if (nxt < num_tiles)
+            scan_tile(p, nxt, tag, abuf(q + 1), abuf(q + 1) + kTile, &sh.bar[(q + 1) % kBufs],
+                      (q + 1) / kBufs, sh.warp_agg, &sh.tagg[1], rn);
+        __syncthreads();
+        unsigned after = sh.tick[q % kBufs];
+        fix_up(p, cur, abuf(q), abuf(q) + kTile, rc, sh.carry);
+        compute_sync();  // tile q's buffer is free
+        if (after < num_tiles) stage_tile(p, after, abuf(q), abuf(q) + kTile, &sh.bar[q % kBufs]);
+        __syncthreads();
+        cur = nxt;
+        nxt = sh.tick[(q + 2) % kBufs];
+        if (cur >= num_tiles) break;
+
+        const unsigned q1 = q + 1;
+        if (nxt < num_tiles)
+            scan_tile(p, nxt, tag, abuf(q1 + 1), abuf(q1 + 1) + kTile, &sh.bar[(q1 + 1) % kBufs],
+                      (q1 + 1) / kBufs, sh.warp_agg, &sh.tagg[0], rc);
+        __syncthreads();
+        after = sh.tick[q1 % kBufs];
+        fix_up(p, cur, abuf(q1), abuf(q1) + kTile, rn, sh.carry);
+        compute_sync();
+        if (after < num_tiles) stage_tile(p, after, abuf(q1), abuf(q1) + kTile, &sh.bar[q1 % kBufs]);
+        __syncthreads();
+        cur = nxt;
+        nxt = sh.tick[(q1 + 2) % kBufs];
+    }
+}
+
+// Persistent, software-pipelined, warp-specialised. Each CTA owns a ring of
+// kBufs tile buffers, 8 compute warps and one control warp. CTA-local tile
+// q (the q-th ticket this CTA took) lives in buffer q % kBufs. Per step q the
+// compute warps scan tile q+1 and publish its aggregate while the control
+// warp looks back for tile q and takes the ticket of tile q+kBufs; then the
+// compute warps fix up and store tile q and refill its buffer with tile
+// q+kBufs. A tile's aggregate never waits on another tile's look-back, and
+// the look-back overlaps the scan. Both loops pass the same two barriers per
+// step and stop at the same step.
+__global__ void __launch_bounds__(kCtaThreads, kBufs == 2 ? 3 : 2)
+affine_scan_kernel(const AffineParams p) {
+    extern __shared__ __align__(128) float s_dyn[];  // [kBufs][a | b][kTile]
+    __shared__ AffineShared sh;
+    __shared__ __align__(16) Pair s_walk[kMaxWindows * 32];
+
+    const unsigned num_tiles = (unsigned)((p.n + kTile - 1) / kTile);
+    if (threadIdx.x == kThreads) {
+        sh.tag = ld_relaxed_u32(&p.ws->epoch) + 1u;
+        for (int i = 0; i < kBufs; ++i) {
+            sh.tick[i] = atomicAdd(&p.ws->ticket, 1u);
+            mbar_init(&sh.bar[i], 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x >= kThreads)
+        control_loop(p, sh, s_walk, num_tiles);
+    else
+        compute_loop(p, sh, s_dyn, num_tiles);
+    finish_launch(p.ws, sh.tag);
 }
 
 }  // namespace
@@ -317,7 +463,22 @@ ss_status affine_launch(const float *a, const float *b, float *h, int64_t n, voi
     prm.skip_unit = skip_unit;
     prm.bulk_ok = ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
     prm.vec_out = (reinterpret_cast<uintptr_t>(h) & 15u) == 0;
-    affine_scan_kernel<<<(unsigned)tiles, kThreads, 0, stream>>>(prm);
+    // persistent grid: as many CTAs as fit at once, capped by the tile count
+    static int ctas_per_sm = -1, sms = 0;
+    if (ctas_per_sm < 0) {
+        int dev = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaFuncSetAttribute(affine_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDynSmem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, affine_scan_kernel, kCtaThreads,
+                                                          kDynSmem) != cudaSuccess ||
+            per_sm < 1)
+            return SS_ERR_CUDA;
+        ctas_per_sm = per_sm;
+    }
+    const long long grid = std::min<long long>(tiles, (long long)sms * ctas_per_sm);
+    affine_scan_kernel<<<(unsigned)grid, kCtaThreads, kDynSmem, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

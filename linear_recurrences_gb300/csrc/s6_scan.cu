@@ -33,9 +33,12 @@
 // with one fma each, in sequence order, starting from the nearest published
 // inclusive state. By induction that equals the inclusive state the
 // predecessor publishes, bit for bit, so results do not depend on timing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 #include <cstdio>
 #include <cstdlib>
 
@@ -61,6 +64,7 @@ enum { F_P = 0, F_H = 1, F_INC = 2, F_HR = 3, F_RINC = 4 };
 enum { FL_AGG = 0, FL_INC = 1, FL_RINC = 2, FL_PAD = 3 };
 
 struct S6Params {
+    CUtensorMap tm_x, tm_d, tm_b, tm_c;  // 2D maps: (D or N) x (B*L rows); valid if tma
     const void *x, *delta, *Bt, *Ct;
     const float *A, *Dskip;
     void *y;
@@ -71,7 +75,7 @@ struct S6Params {
     int K;             // chunks per sequence
     int WT;            // warps per CTA
     int Tsub;          // timesteps per warp
-    int bulk;          // rows and tiles are 16-byte aligned: stage with bulk copies
+    int bulk;          // rows and tiles are 16-byte aligned: stage with TMA tile copies
     WsHeader *ws;
     unsigned *flags;   // [(seq*K + k)*4 + FL_*]
     float *payload;    // [((seq*K + k)*NF + field)*32*NG + lane*NG + i]
@@ -200,20 +204,18 @@ __device__ __forceinline__ void issue_stage(const S6Params &p, WarpCtx &w, int s
     const long long row0 = w.b * p.L + ts;
     const int N = p.N;
     if (p.bulk) {
-        const unsigned xrow = (unsigned)(w.cw * sizeof(IO));
-        const unsigned btile = (unsigned)(nrows * N * sizeof(IO));
-        const unsigned bytes = nrows * 2u * xrow + (MODE == MODE_OUT ? 2u : 1u) * btile;
-        uint64_t *bar = w.bars + slot;
-        if (w.lane == 0) mbar_arrive_expect_tx(bar, bytes);
-        __syncwarp();
-        if (w.lane < nrows) {
-            const long long gi = (row0 + w.lane) * p.D + w.d0;
-            bulk_g2s(xs + w.lane * 32, xg + gi, xrow, bar);
-            bulk_g2s(ds + w.lane * 32, dg + gi, xrow, bar);
-        }
+        // one elected lane: expect the tile bytes, then four 2D tile copies
+        // (boxes past the tensor's end arrive zero-filled and are never used)
         if (w.lane == 0) {
-            bulk_g2s(bs, bg + row0 * N, btile, bar);
-            if (MODE == MODE_OUT) bulk_g2s(cs, cg + row0 * N, btile, bar);
+            const unsigned xbytes = kTS * 32u * (unsigned)sizeof(IO);
+            const unsigned bbytes = kTS * (unsigned)N * (unsigned)sizeof(IO);
+            uint64_t *bar = w.bars + slot;
+            mbar_arrive_expect_tx(bar, 2u * xbytes + (MODE == MODE_OUT ? 2u : 1u) * bbytes);
+            const int row = (int)row0;
+            tma_load_2d(xs, &p.tm_x, (int)w.d0, row, bar);
+            tma_load_2d(ds, &p.tm_d, (int)w.d0, row, bar);
+            tma_load_2d(bs, &p.tm_b, 0, row, bar);
+            if (MODE == MODE_OUT) tma_load_2d(cs, &p.tm_c, 0, row, bar);
         }
     } else {
         // unaligned shapes: plain loads, synchronous
@@ -432,12 +434,13 @@ __device__ int find_anchor(const S6Params &p, long long seq, int k, unsigned tag
 // ------------------------------------------------------------------ kernel
 template <int NG, typename IO, bool SP, bool BIDIR>
 __global__ void __launch_bounds__(kMaxWT * 32)
-s6_kernel(const S6Params p) {
+s6_kernel(const __grid_constant__ S6Params p) {
     constexpr int NSUB = BIDIR ? 3 : 2;  // sub-aggregate fields: P, H (, Hr)
     constexpr int NF = BIDIR ? 5 : 3;    // descriptor fields
     constexpr int NP = NG / 2;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    unsigned char *s_ring = smem_raw;                                       // [WT][Ring::kWarp]
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    // TMA destinations need 128-byte alignment; the launch adds 128 bytes of slack
+    unsigned char *s_ring = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
     uint64_t *s_bars = reinterpret_cast<uint64_t *>(s_ring + p.WT * Ring<IO>::kWarp);  // [WT][kStages]
     float *s_sub = reinterpret_cast<float *>(s_bars + p.WT * kStages);      // [WT][NSUB][32][NG]
     float *s_car = s_sub + p.WT * NSUB * 32 * NG;                           // [2][32][NG]
@@ -687,9 +690,42 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     pl.total = 0;
     if (pl.K > 1 || pl.scratch_bytes) pl.total = kWsHeaderBytes + pl.desc_bytes + pl.scratch_bytes;
     const size_t ring = io_bf16 ? Ring<__nv_bfloat16>::kWarp : Ring<float>::kWarp;
-    pl.smem = (size_t)pl.WT * (ring + kStages * sizeof(uint64_t)) +
+    pl.smem = 128 + (size_t)pl.WT * (ring + kStages * sizeof(uint64_t)) +
               (size_t)(pl.WT * NSUB + 2) * 32 * pl.NG * sizeof(float);
     return pl;
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library does not link libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *sym = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &sym, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(sym);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Row-major 2D map over `rows` rows of `inner` elements, box = box_inner x box_rows.
+bool encode_2d(CUtensorMap *m, const void *base, bool bf16, uint64_t inner, uint64_t rows,
+               uint32_t box_inner, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const uint64_t es = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * es};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int NG, typename IO, bool SP, bool BIDIR>
@@ -762,7 +798,16 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
     const size_t es = a.io_bf16 ? 2 : 4;
     const uintptr_t al = reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.delta) |
                          reinterpret_cast<uintptr_t>(a.Bt) | reinterpret_cast<uintptr_t>(a.Ct);
-    prm.bulk = ((a.D * es) % 16 == 0) && ((a.N * es) % 16 == 0) && (al % 16 == 0);
+    prm.bulk = ((a.D * es) % 16 == 0) && ((a.N * es) % 16 == 0) && (al % 16 == 0) &&
+               (a.B * a.L < (1LL << 31)) && (a.D < (1LL << 31));
+    if (prm.bulk) {
+        const bool bf = a.io_bf16 != 0;
+        const uint64_t rows = (uint64_t)(a.B * a.L);
+        prm.bulk = encode_2d(&prm.tm_x, a.x, bf, a.D, rows, 32, kTS) &&
+                   encode_2d(&prm.tm_d, a.delta, bf, a.D, rows, 32, kTS) &&
+                   encode_2d(&prm.tm_b, a.Bt, bf, a.N, rows, (uint32_t)a.N, kTS) &&
+                   encode_2d(&prm.tm_c, a.Ct, bf, a.N, rows, (uint32_t)a.N, kTS);
+    }
     prm.timeout_ns = timeout_ns;
     prm.skip_unit = skip_unit;
     char *ws = static_cast<char *>(workspace);

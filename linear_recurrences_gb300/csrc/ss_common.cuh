@@ -159,6 +159,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned by
         ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
+// 2D tile copy global -> shared through a tensor map, completing on `bar`.
+// x (innermost coordinate) times the element size must be a multiple of 16
+// bytes; dst 128-byte aligned.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y),
+          "r"(smem_addr(bar)) : "memory");
+}
+
 // Waits for phase `parity` of `bar` for at most `timeout_ns`. Returns false
 // on timeout (the copies it tracks may still be in flight).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity,
