@@ -97,6 +97,35 @@ size_t ss_affine_scan_workspace_bytes(int64_t n);
 ss_status ss_affine_scan(const float *a, const float *b, float *h, int64_t n,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Largest n ss_affine_scan_noalloc accepts (2^24 elements). Its scratch
+ * array is 256 + 32 * (SS_AFFINE_NOALLOC_MAX_N / 4096) = 131,328 bytes.
+ */
+#define SS_AFFINE_NOALLOC_MAX_N (1LL << 24)
+
+/*
+ * ss_affine_scan without a workspace argument, for callers that cannot
+ * allocate device memory (code that runs where cudaMalloc is not allowed or
+ * not safe, such as inside an allocator, a plugin that must leave the device
+ * heap alone, or a path that may not allocate after start-up). The pages
+ * describing the method have no counterpart to this entry point.
+ * Computes the same h as ss_affine_scan (same kernel, same results) for
+ * 0 <= n <= SS_AFFINE_NOALLOC_MAX_N; larger n returns SS_ERR_UNSUPPORTED
+ * with nothing launched. a, b, h: caller-owned device arrays as for
+ * ss_affine_scan; stream: a cudaStream_t.
+ * The scratch it needs lives in one static device array inside the library
+ * (131,328 bytes, reserved on every GPU that loads the library until the
+ * process exits); the call allocates and frees nothing. The first call on a
+ * device looks up that array's device address (cudaGetSymbolAddress), so
+ * make it before any stream capture on that device. Every call uses the same
+ * array: calls that can run at the same time on the GPU (different streams,
+ * or threads without ordering between them) race and must not be made.
+ * Each call clears the array's error word on `stream`; device-detected
+ * errors are not reported for this entry point.
+ */
+ss_status ss_affine_scan_noalloc(const float *a, const float *b, float *h, int64_t n,
+                                 void *stream);
+
 /* ------------------------------------------------------------ S6 */
 
 /* Bytes of workspace the S6 calls need for this shape and storage type on

@@ -26,7 +26,8 @@ __all__ = [
     "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
-    "ss_probe_mufu_ex2", "new_workspace", "EXPORTED_SYMBOLS",
+    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
+    "new_workspace", "EXPORTED_SYMBOLS",
 ]
 
 SS_OK, SS_ERR_INVALID, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -37,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
-    "ss_probe_mufu_ex2",
+    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc",
 )
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -95,6 +96,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_testing_skip_publish_once.restype = None
     L.ss_probe_mufu_ex2.argtypes = [vp, ci, ci, vp]
     L.ss_probe_mufu_ex2.restype = ci
+    L.ss_affine_scan_noalloc.argtypes = [vp, vp, vp, i64, vp]
+    L.ss_affine_scan_noalloc.restype = ci
     return L
 
 
@@ -203,6 +206,28 @@ def ss_affine_scan(a, b, h=None, workspace=None, stream=None):
     st = lib().ss_affine_scan(_ptr(a), _ptr(b), _ptr(h), n, _ptr(workspace), wsb, sh)
     if st != SS_OK:
         raise SSError(st, "ss_affine_scan")
+    return h
+
+
+SS_AFFINE_NOALLOC_MAX_N = 1 << 24
+
+
+def ss_affine_scan_noalloc(a, b, h=None, stream=None):
+    """ss_affine_scan with the library's static scratch array instead of a
+    workspace (for callers that must not allocate device memory; see
+    include/ss.h). n <= SS_AFFINE_NOALLOC_MAX_N."""
+    torch = _torch()
+    _check_cuda(a, "a", (torch.float32,))
+    _check_cuda(b, "b", (torch.float32,))
+    if a.dim() != 1 or a.shape != b.shape or a.device != b.device:
+        raise ValueError("a and b must be 1-D, same length, same device")
+    if h is None:
+        h = torch.empty_like(a)
+    _check_cuda(h, "h", (torch.float32,))
+    st = lib().ss_affine_scan_noalloc(_ptr(a), _ptr(b), _ptr(h), a.numel(),
+                                      _stream_handle(stream, a.device))
+    if st != SS_OK:
+        raise SSError(st, "ss_affine_scan_noalloc")
     return h
 
 

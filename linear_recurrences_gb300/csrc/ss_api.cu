@@ -53,6 +53,10 @@ ss_status s6_entry(const void *x, const void *delta, const void *Bt, const void 
 
 }  // namespace
 
+namespace ss {
+unsigned long long spin_timeout_ns() { return g_timeout_ns.load(); }
+}  // namespace ss
+
 extern "C" {
 
 const char *ss_status_string(int status) {

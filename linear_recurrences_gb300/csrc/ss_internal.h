@@ -23,6 +23,9 @@ struct S6Args {
     int bidir;
 };
 
+// Current bound on device-side waits (ss_set_spin_timeout_ns).
+unsigned long long spin_timeout_ns();
+
 size_t s6_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir);
 ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStream_t stream,
                     unsigned long long timeout_ns, long long skip_unit);
