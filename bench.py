@@ -129,6 +129,18 @@ class ClockSampler:
                                                          if r[3].replace(".", "").isdigit())}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest `value` over the ranks of the default process group (the job's
+    time is its slowest rank's); returns `value` when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- device timing
 def time_launches(torch, fn, steps, warmup, stream, flush=None, barrier=None):
     """Per-launch CUDA-event durations (ms) of `fn` over `steps` timed calls,
@@ -334,12 +346,7 @@ def run_ours(args, rank, world, local_rank):
     if status != ss.SS_OK:
         raise RuntimeError(f"device reported {ss.ss_status_string(status)}")
     clocks = clk.summary()
-    region_ms_all = region_ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([region_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        region_ms_all = float(t.item())
+    region_ms_all = max_over_ranks(region_ms, dev)
     elems = w.n * args.steps * world
     value = elems / (region_ms_all * 1e-3)
     launch_ms = statistics.mean(per)
@@ -360,7 +367,7 @@ def run_ours(args, rank, world, local_rank):
 
     e2e_per, e2e_region = time_launches(torch, e2e_step, max(3, args.steps // 4),
                                         min(args.warmup, 3), stream, barrier=barrier)
-    e2e_value = w.n * len(e2e_per) * world / (e2e_region * 1e-3)
+    e2e_value = w.n * len(e2e_per) * world / (max_over_ranks(e2e_region, dev) * 1e-3)
 
     extras = {}
     if rank == 0 and not args.no_extras:
