@@ -50,10 +50,9 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kMaxWT = 8;       // warps per CTA along time (hard limit)
+constexpr int kMaxWT = 4;       // warps per CTA along time (hard limit)
 constexpr int kDefaultWT = 4;   // default: small CTAs so several fit per SM
 constexpr int kMaxWindows = 4;  // look-back holds up to 128 predecessor chunks
-constexpr int kTS = 8;          // timesteps per ring stage
 constexpr int kStages = 3;      // ring slots per warp
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kCopyTimeoutNs = 2000000000ull;
@@ -105,6 +104,11 @@ __device__ __forceinline__ u64 f2mul(u64 a, u64 b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
+__device__ __forceinline__ u64 f2add(u64 a, u64 b) {
+    u64 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
 __device__ __forceinline__ u64 f2fma(u64 a, u64 b, u64 c) {
     u64 r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
@@ -119,12 +123,14 @@ __device__ __forceinline__ void store_io(__nv_bfloat16 *p, float v) { *p = __flo
 
 // softplus(v) = log(1 + exp(v)); v > 20 returns v. exp and log on MUFU; for
 // exp(v) < 1/64 the log is replaced by its alternating series so that the
-// rounding of 1 + exp(v) does not swamp small results.
+// rounding of 1 + exp(v) does not swamp small results. Both forms are
+// computed and selected, so the step has no branch.
 __device__ __forceinline__ float softplus_mufu(float v) {
-    if (v > 20.0f) return v;
-    const float e = ex2_approx(v * kLog2e);
-    if (e < 0.015625f) return e * (1.0f - e * (0.5f - e * (1.0f / 3.0f - 0.25f * e)));
-    return lg2_approx(1.0f + e) * kLn2;
+    const float e = ex2_approx(fminf(v, 20.0f) * kLog2e);
+    const float series = e * (1.0f - e * (0.5f - e * (1.0f / 3.0f - 0.25f * e)));
+    const float logged = lg2_approx(1.0f + e) * kLn2;
+    const float r = e < 0.015625f ? series : logged;
+    return v > 20.0f ? v : r;
 }
 
 template <int NG>
@@ -163,9 +169,12 @@ __device__ __forceinline__ void publish_flag(const S6Params &p, long long unit, 
 
 // ------------------------------------------------------------------ staging ring
 // Per-warp shared memory: kStages slots of {x rows, delta rows, Bt tile, Ct
-// tile} in the storage type, then fp32 copies of the current Bt / Ct rows
-// padded to 16 states (used for bf16 storage or N != NG).
+// tile} of kTS timesteps in the storage type, then fp32 copies of the current
+// Bt / Ct rows padded to 16 states (used for bf16 storage or N != NG). bf16
+// stages hold twice the timesteps, so the per-stage work (copy issue, wait,
+// widening) is spread over more steps in the same shared memory.
 template <typename IO> struct Ring {
+    static constexpr int kTS = sizeof(IO) == 2 ? 16 : 8;
     static constexpr int kXBytes = kTS * 32 * (int)sizeof(IO);
     static constexpr int kBBytes = kTS * 16 * (int)sizeof(IO);
     static constexpr int kSlot = 2 * kXBytes + 2 * kBBytes;
@@ -176,10 +185,13 @@ template <typename IO> struct Ring {
 struct WarpCtx {
     unsigned char *ring;   // this warp's ring
     uint64_t *bars;        // this warp's kStages mbarriers
-    unsigned issued;       // stage loads issued so far (all sweeps)
+    int slot;              // next ring slot to consume (and to refill after it)
+    unsigned phases;       // bit s: parity of slot s's next completion
     long long b, d0, d;
     int cw;                // valid channels in this warp's tile
     int lane;
+    int ch;                // channel of this lane within the warp's tile
+    int half;              // which NG-state slice of the channel this lane holds
     bool dvalid;
     long long t0, t1;      // this warp's timesteps
 };
@@ -187,9 +199,11 @@ struct WarpCtx {
 enum { MODE_AGG = 0, MODE_OUT = 1 };
 
 // Starts loading stage `st` (timesteps t0 + st*kTS ...) into `slot`.
-template <typename IO, int MODE>
+template <typename IO, int MODE, int LPC>
 __device__ __forceinline__ void issue_stage(const S6Params &p, WarpCtx &w, int st, int slot) {
+    constexpr int CPW = 32 / LPC;  // channels per warp
     using R = Ring<IO>;
+    constexpr int kTS = R::kTS;
     const long long ts = w.t0 + (long long)st * kTS;
     const int nrows = (int)min((long long)kTS, w.t1 - ts);
     unsigned char *sl = w.ring + slot * R::kSlot;
@@ -207,7 +221,7 @@ __device__ __forceinline__ void issue_stage(const S6Params &p, WarpCtx &w, int s
         // one elected lane: expect the tile bytes, then four 2D tile copies
         // (boxes past the tensor's end arrive zero-filled and are never used)
         if (w.lane == 0) {
-            const unsigned xbytes = kTS * 32u * (unsigned)sizeof(IO);
+            const unsigned xbytes = kTS * (unsigned)CPW * (unsigned)sizeof(IO);
             const unsigned bbytes = kTS * (unsigned)N * (unsigned)sizeof(IO);
             uint64_t *bar = w.bars + slot;
             mbar_arrive_expect_tx(bar, 2u * xbytes + (MODE == MODE_OUT ? 2u : 1u) * bbytes);
@@ -219,10 +233,12 @@ __device__ __forceinline__ void issue_stage(const S6Params &p, WarpCtx &w, int s
         }
     } else {
         // unaligned shapes: plain loads, synchronous
-        for (int r = 0; r < nrows; ++r) {
-            const long long gi = (row0 + r) * p.D + w.d;
-            xs[r * 32 + w.lane] = w.dvalid ? xg[gi] : IO(0.0f);
-            ds[r * 32 + w.lane] = w.dvalid ? dg[gi] : IO(0.0f);
+        if (w.half == 0) {
+            for (int r = 0; r < nrows; ++r) {
+                const long long gi = (row0 + r) * p.D + w.d;
+                xs[r * CPW + w.ch] = w.dvalid ? xg[gi] : IO(0.0f);
+                ds[r * CPW + w.ch] = w.dvalid ? dg[gi] : IO(0.0f);
+            }
         }
         for (int i = w.lane; i < nrows * N; i += 32) {
             bs[i] = bg[row0 * N + i];
@@ -233,10 +249,10 @@ __device__ __forceinline__ void issue_stage(const S6Params &p, WarpCtx &w, int s
 }
 
 template <typename IO>
-__device__ __forceinline__ void wait_stage(const S6Params &p, WarpCtx &w, unsigned idx) {
+__device__ __forceinline__ void wait_stage(const S6Params &p, WarpCtx &w, int slot) {
     if (!p.bulk) return;
-    const int slot = idx % kStages;
-    const unsigned parity = (idx / kStages) & 1u;
+    const unsigned parity = (w.phases >> slot) & 1u;
+    w.phases ^= 1u << slot;
     if (!mbar_wait_bounded(w.bars + slot, parity, kCopyTimeoutNs)) {
         if (w.lane == 0) record_error(p.ws, SS_ERR_TIMEOUT, 5u, (unsigned)w.b, (unsigned)w.t0);
         mbar_wait_bounded(w.bars + slot, parity, kCopyTimeoutNs);
@@ -264,7 +280,7 @@ __device__ __forceinline__ u64 f2_exp2_scaled(u64 dd, u64 a2) {
 
 // One timestep of this lane's chains. xv, dv: x and delta of (t, d); brow,
 // crow: Bt and Ct rows of t as fp32; yp: this lane's output element.
-template <int NG, typename IO, bool SP, bool BIDIR, int MODE, int OUT>
+template <int NG, int LPC, typename IO, bool SP, bool BIDIR, int MODE, int OUT>
 __device__ __forceinline__ void step(float xv, float dv, const float *brow, const float *crow,
                                      const u64 (&A2)[NG / 2], float Dd, u64 (&h)[NG / 2],
                                      u64 (&hr)[NG / 2], u64 (&Q)[NG / 2], float &sdel, IO *yp,
@@ -303,7 +319,9 @@ __device__ __forceinline__ void step(float xv, float dv, const float *brow, cons
             acc0 = f2fma(h[2 * q4], cq.x, acc0);
             acc1 = f2fma(h[2 * q4 + 1], cq.y, acc1);
         }
-        const float accs = (f2lo(acc0) + f2hi(acc0)) + (f2lo(acc1) + f2hi(acc1));
+        const u64 acc = f2add(acc0, acc1);
+        float accs = f2lo(acc) + f2hi(acc);
+        if constexpr (LPC == 2) accs += __shfl_xor_sync(0xffffffffu, accs, 1);  // other state half
         const float yv = fmaf(Dd, xv, accs);
         if (store) {
             if constexpr (OUT == OUT_Y) store_io(yp, yv);
@@ -313,79 +331,130 @@ __device__ __forceinline__ void step(float xv, float dv, const float *brow, cons
     }
 }
 
+// Widens the stage's Bt (and Ct) rows to fp32 x 16 states in `bconv` /
+// `cconv`. bf16 with N == 16: 16-byte chunks of 8 values spread over the
+// lanes (Bt chunks first, then Ct); other shapes: element by element, padded
+// with zeros.
+template <typename IO, int MODE>
+__device__ __forceinline__ void widen_rows(const WarpCtx &w, const IO *bs, const IO *cs, int nrows,
+                                           int N, float *bconv, float *cconv) {
+    constexpr int kTS = Ring<IO>::kTS;
+    if (sizeof(IO) == 2 && N == 16) {
+        constexpr int kChunks = kTS * 2;  // per matrix
+#pragma unroll
+        for (int i0 = 0; i0 < (MODE == MODE_OUT ? 2 : 1) * kChunks; i0 += 32) {
+            const int i = i0 + w.lane;
+            if (i < (MODE == MODE_OUT ? 2 : 1) * kChunks) {
+                const bool isC = i >= kChunks;
+                const int c = isC ? i - kChunks : i;
+                const uint4 v = *reinterpret_cast<const uint4 *>((isC ? cs : bs) + c * 8);
+                float4 *dst = reinterpret_cast<float4 *>((isC ? cconv : bconv) + c * 8);
+                dst[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+                dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                                     __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+            }
+        }
+    } else {
+        for (int i = w.lane; i < nrows * 16; i += 32) {
+            const int r = i >> 4, n = i & 15;
+            bconv[i] = n < N ? to_f32(bs[r * N + n]) : 0.0f;
+            if (MODE == MODE_OUT) cconv[i] = n < N ? to_f32(cs[r * N + n]) : 0.0f;
+        }
+    }
+    __syncwarp();
+}
+
+// Issues the first ring stages of a pass (up to kStages) starting at the
+// warp's next slot, so that they can land while the warp does other work.
+template <typename IO, int MODE, int LPC, bool REV>
+__device__ __forceinline__ void sweep_prime(const S6Params &p, WarpCtx &w) {
+    constexpr int kTS = Ring<IO>::kTS;
+    const long long len = w.t1 - w.t0;
+    if (len <= 0) return;
+    const int nst = (int)((len + kTS - 1) / kTS);
+    const int pre = min(kStages, nst);
+    int sl = w.slot;
+    for (int q = 0; q < pre; ++q) {
+        issue_stage<IO, MODE, LPC>(p, w, REV ? nst - 1 - q : q, sl);
+        sl = sl == kStages - 1 ? 0 : sl + 1;
+    }
+}
+
 // One pass of this lane's chains over its timesteps, streamed through the ring.
 // MODE_AGG: from the state in h (zero), accumulate the sub-chunk aggregate.
 // MODE_OUT: from the state in h, write outputs (OUT_* above).
-template <int NG, typename IO, bool SP, bool BIDIR, int MODE, bool REV, int OUT>
+// PRIMED: sweep_prime already issued the first stages.
+// Every stage a pass issues is consumed by the same pass, in issue order, so
+// the ring's next slot carries over from one pass to the next.
+template <int NG, int LPC, typename IO, bool SP, bool BIDIR, int MODE, bool REV, int OUT,
+          bool PRIMED = false>
 __device__ __forceinline__ void sweep(const S6Params &p, WarpCtx &w, const u64 (&A2)[NG / 2],
                                       float Dd, u64 (&h)[NG / 2], u64 (&hr)[NG / 2],
                                       u64 (&Q)[NG / 2], float &sdel, float *yf) {
     using R = Ring<IO>;
+    constexpr int kTS = R::kTS;
     const long long len = w.t1 - w.t0;
     if (len <= 0) return;
     const int nst = (int)((len + kTS - 1) / kTS);
+    constexpr int CPW = 32 / LPC;
     const int N = p.N;
-    const bool conv = (sizeof(IO) == 2) || (N != NG);
+    const bool conv = (sizeof(IO) == 2) || (N != NG * LPC);
     float *bconv = reinterpret_cast<float *>(w.ring + kStages * R::kSlot);
     float *cconv = bconv + kTS * 16;
-    const unsigned base = w.issued;
-    const int pre = min(kStages, nst);
-    for (int q = 0; q < pre; ++q) issue_stage<IO, MODE>(p, w, REV ? nst - 1 - q : q, (base + q) % kStages);
-    w.issued += pre;
+    if (!PRIMED) sweep_prime<IO, MODE, LPC, REV>(p, w);
     const long long D = p.D;
     IO *ybase = static_cast<IO *>(p.y) + w.b * p.L * D + w.d;   // y[b, 0, d]
     float *yfbase = yf ? yf + w.b * p.L * D + w.d : nullptr;
+    const bool store = w.dvalid && w.half == 0;
+    const int bstride = conv ? 16 : N;
 
+    int slot = w.slot;
     for (int q = 0; q < nst; ++q) {
-        const unsigned idx = base + q;
-        const int slot = idx % kStages;
         const int st = REV ? nst - 1 - q : q;
-        wait_stage<IO>(p, w, idx);
+        wait_stage<IO>(p, w, slot);
         const unsigned char *sl = w.ring + slot * R::kSlot;
-        const IO *xs = reinterpret_cast<const IO *>(sl) + w.lane;
-        const IO *ds = reinterpret_cast<const IO *>(sl + R::kXBytes) + w.lane;
+        const IO *xs = reinterpret_cast<const IO *>(sl) + w.ch;
+        const IO *ds = reinterpret_cast<const IO *>(sl + R::kXBytes) + w.ch;
         const IO *bs = reinterpret_cast<const IO *>(sl + 2 * R::kXBytes);
         const IO *cs = reinterpret_cast<const IO *>(sl + 2 * R::kXBytes + R::kBBytes);
         const long long ts = w.t0 + (long long)st * kTS;
         const int nrows = (int)min((long long)kTS, w.t1 - ts);
-        if (conv) {
-            // widen / pad the stage's Bt (and Ct) rows to fp32 x 16 states
-            for (int i = w.lane; i < nrows * 16; i += 32) {
-                const int r = i >> 4, n = i & 15;
-                bconv[i] = n < N ? to_f32(bs[r * N + n]) : 0.0f;
-                if (MODE == MODE_OUT) cconv[i] = n < N ? to_f32(cs[r * N + n]) : 0.0f;
-            }
-            __syncwarp();
-        }
-        const float *bf = conv ? bconv : reinterpret_cast<const float *>(bs);
-        const float *cf = conv ? cconv : reinterpret_cast<const float *>(cs);
-        const int bstride = conv ? 16 : NG;
+        if (conv) widen_rows<IO, MODE>(w, bs, cs, nrows, N, bconv, cconv);
+        // this lane's state slice of each Bt / Ct row
+        const float *bf = (conv ? bconv : reinterpret_cast<const float *>(bs)) + w.half * NG;
+        const float *cf = (conv ? cconv : reinterpret_cast<const float *>(cs)) + w.half * NG;
         IO *yp = ybase + ts * D;
         float *yfp = yfbase ? yfbase + ts * D : nullptr;
         if (nrows == kTS) {
+            // unrolled 8 steps at a time: a fully unrolled 16-step body of
+            // every variant does not fit the instruction cache
+#pragma unroll 1
+            for (int r0 = 0; r0 < kTS; r0 += 8) {
 #pragma unroll
-            for (int rr = 0; rr < kTS; ++rr) {
-                const int r = REV ? kTS - 1 - rr : rr;
-                step<NG, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * 32]), to_f32(ds[r * 32]),
-                                                   bf + r * bstride, cf + r * bstride, A2, Dd, h,
-                                                   hr, Q, sdel, yp + r * D,
-                                                   yfp ? yfp + r * D : nullptr, w.dvalid);
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int r = REV ? kTS - 1 - (r0 + rr) : r0 + rr;
+                    step<NG, LPC, IO, SP, BIDIR, MODE, OUT>(
+                        to_f32(xs[r * CPW]), to_f32(ds[r * CPW]), bf + r * bstride,
+                        cf + r * bstride, A2, Dd, h, hr, Q, sdel, yp + r * D,
+                        yfp ? yfp + r * D : nullptr, store);
+                }
             }
         } else {
             for (int rr = 0; rr < nrows; ++rr) {
                 const int r = REV ? nrows - 1 - rr : rr;
-                step<NG, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * 32]), to_f32(ds[r * 32]),
-                                                   bf + r * bstride, cf + r * bstride, A2, Dd, h,
-                                                   hr, Q, sdel, yp + r * D,
-                                                   yfp ? yfp + r * D : nullptr, w.dvalid);
+                step<NG, LPC, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * CPW]), to_f32(ds[r * CPW]),
+                                                        bf + r * bstride, cf + r * bstride, A2, Dd,
+                                                        h, hr, Q, sdel, yp + r * D,
+                                                        yfp ? yfp + r * D : nullptr, store);
             }
         }
         __syncwarp();  // every lane is done with this slot (and the fp32 rows)
-        if (q + kStages < nst) {
-            issue_stage<IO, MODE>(p, w, REV ? nst - 1 - (q + kStages) : q + kStages, slot);
-            w.issued += 1;
-        }
+        if (q + kStages < nst)
+            issue_stage<IO, MODE, LPC>(p, w, REV ? nst - 1 - (q + kStages) : q + kStages, slot);
+        slot = slot == kStages - 1 ? 0 : slot + 1;
     }
+    w.slot = slot;
 }
 
 // ------------------------------------------------------------------ look-back
@@ -431,10 +500,39 @@ __device__ int find_anchor(const S6Params &p, long long seq, int k, unsigned tag
     }
 }
 
+// Applies the aggregates of chunks m = from, from + dir, ... (stopping before
+// `to`) to the state c, one fma per state each, in that order. The next
+// chunk's aggregate is loaded while the current one is applied, so the walk
+// costs about one L2 round trip per chunk only when it is a single chunk.
+template <int NG>
+__device__ __forceinline__ void apply_aggregates(const S6Params &p, int NF, long long seq, int from,
+                                                 int to, int dir, int fieldH, int lane,
+                                                 float (&c)[NG]) {
+    if (from == to) return;
+    float Pn[NG], Hn[NG];
+    load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + from, F_P, lane), Pn);
+    load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + from, fieldH, lane), Hn);
+    for (int m = from; m != to; m += dir) {
+        float Pm[NG], Hm[NG];
+#pragma unroll
+        for (int i = 0; i < NG; ++i) {
+            Pm[i] = Pn[i];
+            Hm[i] = Hn[i];
+        }
+        if (m + dir != to) {
+            load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m + dir, F_P, lane), Pn);
+            load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m + dir, fieldH, lane), Hn);
+        }
+#pragma unroll
+        for (int i = 0; i < NG; ++i) c[i] = fmaf(Pm[i], c[i], Hm[i]);
+    }
+}
+
 // ------------------------------------------------------------------ kernel
-template <int NG, typename IO, bool SP, bool BIDIR>
-__global__ void __launch_bounds__(kMaxWT * 32)
+template <int NG, int LPC, typename IO, bool SP, bool BIDIR>
+__global__ void __launch_bounds__(kMaxWT * 32, 3)
 s6_kernel(const __grid_constant__ S6Params p) {
+    constexpr int CPW = 32 / LPC;  // channels per warp
     constexpr int NSUB = BIDIR ? 3 : 2;  // sub-aggregate fields: P, H (, Hr)
     constexpr int NF = BIDIR ? 5 : 3;    // descriptor fields
     constexpr int NP = NG / 2;
@@ -460,13 +558,16 @@ s6_kernel(const __grid_constant__ S6Params p) {
     WarpCtx w;
     w.ring = s_ring + warp * Ring<IO>::kWarp;
     w.bars = s_bars + warp * kStages;
-    w.issued = 0;
+    w.slot = 0;
+    w.phases = 0;
     w.lane = lane;
+    w.ch = lane / LPC;
+    w.half = lane % LPC;
     w.b = seq / p.dtiles;
-    w.d0 = (seq % p.dtiles) * 32;
-    w.d = w.d0 + lane;
+    w.d0 = (seq % p.dtiles) * CPW;
+    w.d = w.d0 + w.ch;
     w.dvalid = w.d < p.D;
-    w.cw = (int)min(32LL, p.D - w.d0);
+    w.cw = (int)min((long long)CPW, p.D - w.d0);
     const long long tc0 = (long long)k * p.WT * p.Tsub;
     w.t0 = min(tc0 + (long long)warp * p.Tsub, p.L);
     w.t1 = min(w.t0 + (long long)p.Tsub, p.L);
@@ -479,9 +580,10 @@ s6_kernel(const __grid_constant__ S6Params p) {
     u64 A2[NP];
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
+        const int n0 = w.half * NG + 2 * q;  // this lane's states n0, n0 + 1
         float lo = 0.0f, hi = 0.0f;
-        if (w.dvalid && 2 * q < p.N) lo = p.A[w.d * p.N + 2 * q] * kLog2e;
-        if (w.dvalid && 2 * q + 1 < p.N) hi = p.A[w.d * p.N + 2 * q + 1] * kLog2e;
+        if (w.dvalid && n0 < p.N) lo = p.A[w.d * p.N + n0] * kLog2e;
+        if (w.dvalid && n0 + 1 < p.N) hi = p.A[w.d * p.N + n0 + 1] * kLog2e;
         A2[q] = f2(lo, hi);
     }
     const float Dd = (w.dvalid && p.Dskip) ? p.Dskip[w.d] : 0.0f;
@@ -500,7 +602,7 @@ s6_kernel(const __grid_constant__ S6Params p) {
             hr[q] = 0ull;
             Q[q] = f2(1.0f, 1.0f);
         }
-        sweep<NG, IO, SP, BIDIR, MODE_AGG, false, OUT_Y>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
+        sweep<NG, LPC, IO, SP, BIDIR, MODE_AGG, false, OUT_Y>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
         // s_sub[((w*NSUB + field)*NG + i)*32 + lane]: lane-fastest, conflict-free
         float *mine = s_sub + warp * NSUB * NG * 32 + lane;
 #pragma unroll
@@ -514,6 +616,8 @@ s6_kernel(const __grid_constant__ S6Params p) {
                 mine[(2 * NG + 2 * q + 1) * 32] = f2hi(hr[q]);
             }
         }
+        // the output pass's first stages load while the carries are found
+        sweep_prime<IO, MODE_OUT, LPC, false>(p, w);
         __syncthreads();
 
         if (warp == 0) {
@@ -555,13 +659,7 @@ s6_kernel(const __grid_constant__ S6Params p) {
                     if (lane == 0) record_error(p.ws, SS_ERR_TIMEOUT, 3u, (unsigned)unit, 0u);
                 } else {
                     if (j >= 0) load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + j, F_INC, lane), cf);
-                    for (int m = j + 1; m < k; ++m) {
-                        float Pm[NG], Hm[NG];
-                        load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m, F_P, lane), Pm);
-                        load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m, F_H, lane), Hm);
-#pragma unroll
-                        for (int i = 0; i < NG; ++i) cf[i] = fmaf(Pm[i], cf[i], Hm[i]);
-                    }
+                    apply_aggregates<NG>(p, NF, seq, j + 1, k, 1, F_H, lane, cf);
                 }
                 float inc[NG];
 #pragma unroll
@@ -577,13 +675,7 @@ s6_kernel(const __grid_constant__ S6Params p) {
                     } else {
                         if (jr < p.K)
                             load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + jr, F_RINC, lane), cr);
-                        for (int m = jr - 1; m > k; --m) {
-                            float Pm[NG], Hm[NG];
-                            load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m, F_P, lane), Pm);
-                            load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m, F_HR, lane), Hm);
-#pragma unroll
-                            for (int i = 0; i < NG; ++i) cr[i] = fmaf(Pm[i], cr[i], Hm[i]);
-                        }
+                        apply_aggregates<NG>(p, NF, seq, jr - 1, k, -1, F_HR, lane, cr);
                     }
 #pragma unroll
                     for (int i = 0; i < NG; ++i) inc[i] = fmaf(Pc[i], cr[i], Hrc[i]);
@@ -623,14 +715,21 @@ s6_kernel(const __grid_constant__ S6Params p) {
     // ---- outputs: forward sweep from the carry (and the reverse sweep)
 #pragma unroll
     for (int q = 0; q < NP; ++q) h[q] = f2(cf[2 * q], cf[2 * q + 1]);
+    const bool primed = chunked || p.WT > 1;
     if constexpr (BIDIR) {
         float *yf = p.yscratch ? p.yscratch : static_cast<float *>(p.y);
-        sweep<NG, IO, SP, BIDIR, MODE_OUT, false, OUT_HALF>(p, w, A2, Dd, h, hr, Q, sdel, yf);
+        if (primed)
+            sweep<NG, LPC, IO, SP, BIDIR, MODE_OUT, false, OUT_HALF, true>(p, w, A2, Dd, h, hr, Q, sdel, yf);
+        else
+            sweep<NG, LPC, IO, SP, BIDIR, MODE_OUT, false, OUT_HALF>(p, w, A2, Dd, h, hr, Q, sdel, yf);
 #pragma unroll
         for (int q = 0; q < NP; ++q) h[q] = f2(cr[2 * q], cr[2 * q + 1]);
-        sweep<NG, IO, SP, BIDIR, MODE_OUT, true, OUT_SUM>(p, w, A2, Dd, h, hr, Q, sdel, yf);
+        sweep<NG, LPC, IO, SP, BIDIR, MODE_OUT, true, OUT_SUM>(p, w, A2, Dd, h, hr, Q, sdel, yf);
     } else {
-        sweep<NG, IO, SP, BIDIR, MODE_OUT, false, OUT_Y>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
+        if (primed)
+            sweep<NG, LPC, IO, SP, BIDIR, MODE_OUT, false, OUT_Y, true>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
+        else
+            sweep<NG, LPC, IO, SP, BIDIR, MODE_OUT, false, OUT_Y>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
     }
 
     if (chunked) finish_launch(p.ws, tag);
@@ -638,7 +737,7 @@ s6_kernel(const __grid_constant__ S6Params p) {
 
 // ------------------------------------------------------------------ planning
 struct Plan {
-    int NG, WT, K, Tsub, dtiles;
+    int NG, LPC, WT, K, Tsub, dtiles;
     long long seqs;
     size_t flag_bytes, payload_bytes, scratch_bytes, desc_bytes, total;
     size_t smem;
@@ -656,17 +755,36 @@ int device_sm_count() {
 
 Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir) {
     Plan pl{};
-    pl.NG = N <= 4 ? 4 : (N <= 8 ? 8 : 16);
-    pl.dtiles = (int)((D + 31) / 32);
-    pl.seqs = B * pl.dtiles;
     const long long sms = device_sm_count();
+    pl.NG = N <= 4 ? 4 : (N <= 8 ? 8 : 16);
+    pl.LPC = 1;
+    // Two lanes per channel (8 states each) doubles the warps but repeats the
+    // per-timestep scalar work on both lanes; measured slower on every S6
+    // shape tried, so it is only taken on request.
+    if (const char *e = std::getenv("SS_S6_LPC")) {  // tuning override: 1 or 2
+        if (std::atoi(e) == 2 && pl.NG == 16) {
+            pl.NG = 8;
+            pl.LPC = 2;
+        }
+    }
+    const int cpw = 32 / pl.LPC;
+    pl.dtiles = (int)((D + cpw - 1) / cpw);
+    pl.seqs = B * pl.dtiles;
     const long long target_warps = sms * 16;
     long long S = (target_warps + pl.seqs - 1) / std::max<long long>(pl.seqs, 1);
     S = std::max<long long>(1, std::min<long long>(S, (L + 31) / 32));
     int WT = (int)std::min<long long>(S, kDefaultWT);
     long long K = (S + WT - 1) / WT;
     long long Tsub = (L + K * WT - 1) / (K * WT);
+    const int kTS = io_bf16 ? Ring<__nv_bfloat16>::kTS : Ring<float>::kTS;
     Tsub = (Tsub + kTS - 1) / kTS * kTS;
+    // once L is split at all (two sweeps), at most 128 steps per warp: shorter
+    // chunks keep a chunk's inputs in L2 between its two sweeps and give the
+    // look-back more chunks to overlap
+    if (K * WT > 1) Tsub = std::min<long long>(Tsub, 128);
+    // a bidirectional sequence needs all of its chunks resident at once:
+    // keep K within one chunk per SM
+    if (bidir) Tsub = std::max<long long>(Tsub, (L + (long long)WT * sms - 1) / ((long long)WT * sms));
     if (const char *e = std::getenv("SS_S6_WT_TSUB")) {  // tuning override "WT,Tsub"
         int wv = 0, tv = 0;
         if (std::sscanf(e, "%d,%d", &wv, &tv) == 2 && wv >= 1 && wv <= kMaxWT && tv >= 1) {
@@ -728,9 +846,9 @@ bool encode_2d(CUtensorMap *m, const void *base, bool bf16, uint64_t inner, uint
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NG, typename IO, bool SP, bool BIDIR>
+template <int NG, int LPC, typename IO, bool SP, bool BIDIR>
 ss_status launch_t(const S6Params &prm, const Plan &pl, cudaStream_t stream) {
-    auto kern = s6_kernel<NG, IO, SP, BIDIR>;
+    auto kern = s6_kernel<NG, LPC, IO, SP, BIDIR>;
     if (pl.smem > 48 * 1024) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
             cudaSuccess)
@@ -750,18 +868,22 @@ ss_status launch_t(const S6Params &prm, const Plan &pl, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
-template <int NG, typename IO>
+template <int NG, int LPC, typename IO>
 ss_status launch_ng(const S6Params &prm, const Plan &pl, bool sp, bool bidir, cudaStream_t s) {
-    if (bidir) return sp ? launch_t<NG, IO, true, true>(prm, pl, s) : launch_t<NG, IO, false, true>(prm, pl, s);
-    return sp ? launch_t<NG, IO, true, false>(prm, pl, s) : launch_t<NG, IO, false, false>(prm, pl, s);
+    if (bidir)
+        return sp ? launch_t<NG, LPC, IO, true, true>(prm, pl, s)
+                  : launch_t<NG, LPC, IO, false, true>(prm, pl, s);
+    return sp ? launch_t<NG, LPC, IO, true, false>(prm, pl, s)
+              : launch_t<NG, LPC, IO, false, false>(prm, pl, s);
 }
 
 template <typename IO>
 ss_status launch_io(const S6Params &prm, const Plan &pl, bool sp, bool bidir, cudaStream_t s) {
+    if (pl.LPC == 2) return launch_ng<8, 2, IO>(prm, pl, sp, bidir, s);
     switch (pl.NG) {
-        case 4: return launch_ng<4, IO>(prm, pl, sp, bidir, s);
-        case 8: return launch_ng<8, IO>(prm, pl, sp, bidir, s);
-        default: return launch_ng<16, IO>(prm, pl, sp, bidir, s);
+        case 4: return launch_ng<4, 1, IO>(prm, pl, sp, bidir, s);
+        case 8: return launch_ng<8, 1, IO>(prm, pl, sp, bidir, s);
+        default: return launch_ng<16, 1, IO>(prm, pl, sp, bidir, s);
     }
 }
 
@@ -803,8 +925,10 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
     if (prm.bulk) {
         const bool bf = a.io_bf16 != 0;
         const uint64_t rows = (uint64_t)(a.B * a.L);
-        prm.bulk = encode_2d(&prm.tm_x, a.x, bf, a.D, rows, 32, kTS) &&
-                   encode_2d(&prm.tm_d, a.delta, bf, a.D, rows, 32, kTS) &&
+        const uint32_t cpw = 32u / (uint32_t)pl.LPC;
+        const uint32_t kTS = bf ? Ring<__nv_bfloat16>::kTS : Ring<float>::kTS;
+        prm.bulk = encode_2d(&prm.tm_x, a.x, bf, a.D, rows, cpw, kTS) &&
+                   encode_2d(&prm.tm_d, a.delta, bf, a.D, rows, cpw, kTS) &&
                    encode_2d(&prm.tm_b, a.Bt, bf, a.N, rows, (uint32_t)a.N, kTS) &&
                    encode_2d(&prm.tm_c, a.Ct, bf, a.N, rows, (uint32_t)a.N, kTS);
     }

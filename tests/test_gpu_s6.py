@@ -86,7 +86,7 @@ def test_small_shapes(torch, ss, shape, io, softplus, bidir):
 
 
 @pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
-@pytest.mark.parametrize("wt,tsub", [(1, 3), (1, 7), (2, 8), (3, 5), (8, 4), (4, 33), (8, 64)])
+@pytest.mark.parametrize("wt,tsub", [(1, 3), (1, 7), (2, 8), (3, 5), (4, 4), (4, 33), (4, 64)])
 def test_chunk_splits(torch, ss, plan_override, wt, tsub, bidir):
     """Forces many chunks and sub-chunks so the look-back, the look-forward
     and the in-CTA folds run across ragged boundaries."""
@@ -195,3 +195,32 @@ def test_timeout_is_reported_not_hung(torch, ss, plan_override, bidir):
     fn(*args, y=out, workspace=ws)
     assert ss.ss_get_device_status(ws) == ss.SS_OK
     assert rel_err(to_host_f64(out), oracle_run(inp, False, bidir)) <= TOL["f32"]
+
+
+@pytest.fixture
+def lane_layout():
+    """Forces one or two lanes per channel (SS_S6_LPC) for one test."""
+    old = os.environ.get("SS_S6_LPC")
+
+    def set_(v):
+        os.environ["SS_S6_LPC"] = str(v)
+    yield set_
+    if old is None:
+        os.environ.pop("SS_S6_LPC", None)
+    else:
+        os.environ["SS_S6_LPC"] = old
+
+
+@pytest.mark.parametrize("lpc", [1, 2])
+@pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
+@pytest.mark.parametrize("io,softplus", [("f32", False), ("bf16", True)])
+def test_both_lane_layouts(torch, ss, lane_layout, plan_override, lpc, bidir, io, softplus):
+    """16 states per lane, or 8 states on each of two lanes per channel; the
+    register path (one warp over all of L) and a chunked plan."""
+    lane_layout(lpc)
+    for wt_tsub in (None, (2, 24)):
+        if wt_tsub:
+            plan_override(*wt_tsub)
+        inp = small(2, 333, 70, 16, io=io, softplus=softplus, seed=7 + lpc)
+        y = gpu_run(ss, torch, inp, softplus, bidir)
+        assert rel_err(y, oracle_run(inp, softplus, bidir)) <= TOL[io]
