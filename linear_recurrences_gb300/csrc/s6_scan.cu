@@ -53,7 +53,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxWT = 4;       // warps per CTA along time (hard limit)
 constexpr int kDefaultWT = 4;   // default: small CTAs so several fit per SM
 constexpr int kMaxWindows = 4;  // look-back holds up to 128 predecessor chunks
-constexpr int kStages = 3;      // ring slots per warp
+constexpr int kMaxStages = 3;   // ring slots (and mbarriers) per warp, at most
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kCopyTimeoutNs = 2000000000ull;
 
@@ -139,32 +139,22 @@ __device__ __forceinline__ float *field_ptr(const S6Params &p, int NF, long long
     return p.payload + ((unit * NF + field) * 32 + lane) * NG;
 }
 
-template <int NG>
-__device__ __forceinline__ void store_field(float *dst, const float (&v)[NG]) {
-#pragma unroll
-    for (int q = 0; q < NG / 4; ++q)
-        __stcg(reinterpret_cast<float4 *>(dst) + q,
-               make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
-}
-template <int NG>
-__device__ __forceinline__ void load_field(const float *src, float (&v)[NG]) {
-#pragma unroll
-    for (int q = 0; q < NG / 4; ++q) {
-        const float4 f = ld_cg_f32x4(reinterpret_cast<const float4 *>(src) + q);
-        v[4 * q] = f.x;
-        v[4 * q + 1] = f.y;
-        v[4 * q + 2] = f.z;
-        v[4 * q + 3] = f.w;
-    }
+// Publishes flag `which` of `unit` once every thread of the CTA has written
+// its part of the payload (each thread fences its own writes first).
+__device__ __forceinline__ void publish_cta(const S6Params &p, long long unit, int which,
+                                            unsigned tag) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0 && unit != p.skip_unit) st_release_u32(p.flags + unit * 4 + which, tag);
 }
 
-// Publishes flag `which` of `unit` after every lane of the warp has written
-// its payload (each lane fences its own writes first).
-__device__ __forceinline__ void publish_flag(const S6Params &p, long long unit, int which,
-                                             unsigned tag, int lane) {
-    __threadfence();
-    __syncwarp();
-    if (lane == 0 && unit != p.skip_unit) st_release_u32(p.flags + unit * 4 + which, tag);
+// Four consecutive states (a quad) of one lane's payload field.
+__device__ __forceinline__ float4 *quad_ptr(float *field, int qd) {
+    return reinterpret_cast<float4 *>(field) + qd;
+}
+__device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {
+    return make_float4(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y), fmaf(a.z, b.z, c.z),
+                       fmaf(a.w, b.w, c.w));
 }
 
 // ------------------------------------------------------------------ staging ring
@@ -179,12 +169,14 @@ template <typename IO> struct Ring {
     static constexpr int kBBytes = kTS * 16 * (int)sizeof(IO);
     static constexpr int kSlot = 2 * kXBytes + 2 * kBBytes;
     static constexpr int kConv = 2 * kTS * 16 * 4;
+    static constexpr int kStages = 3;
+    static_assert(kStages <= kMaxStages, "one mbarrier per slot");
     static constexpr int kWarp = kStages * kSlot + kConv;
 };
 
 struct WarpCtx {
     unsigned char *ring;   // this warp's ring
-    uint64_t *bars;        // this warp's kStages mbarriers
+    uint64_t *bars;        // this warp's mbarriers, one per ring slot
     int slot;              // next ring slot to consume (and to refill after it)
     unsigned phases;       // bit s: parity of slot s's next completion
     long long b, d0, d;
@@ -284,7 +276,7 @@ template <int NG, int LPC, typename IO, bool SP, bool BIDIR, int MODE, int OUT>
 __device__ __forceinline__ void step(float xv, float dv, const float *brow, const float *crow,
                                      const u64 (&A2)[NG / 2], float Dd, u64 (&h)[NG / 2],
                                      u64 (&hr)[NG / 2], u64 (&Q)[NG / 2], float &sdel, IO *yp,
-                                     float *yfp, bool store) {
+                                     float *yfp, float yfv, bool store) {
     const float dl = SP ? softplus_mufu(dv) : dv;
     const float u = dl * xv;
     const u64 dd = f2(dl, dl);
@@ -326,7 +318,7 @@ __device__ __forceinline__ void step(float xv, float dv, const float *brow, cons
         if (store) {
             if constexpr (OUT == OUT_Y) store_io(yp, yv);
             else if constexpr (OUT == OUT_HALF) *yfp = yv;
-            else store_io(yp, yv + *yfp);
+            else store_io(yp, yv + yfv);
         }
     }
 }
@@ -370,6 +362,7 @@ __device__ __forceinline__ void widen_rows(const WarpCtx &w, const IO *bs, const
 template <typename IO, int MODE, int LPC, bool REV>
 __device__ __forceinline__ void sweep_prime(const S6Params &p, WarpCtx &w) {
     constexpr int kTS = Ring<IO>::kTS;
+    constexpr int kStages = Ring<IO>::kStages;
     const long long len = w.t1 - w.t0;
     if (len <= 0) return;
     const int nst = (int)((len + kTS - 1) / kTS);
@@ -394,6 +387,7 @@ __device__ __forceinline__ void sweep(const S6Params &p, WarpCtx &w, const u64 (
                                       u64 (&Q)[NG / 2], float &sdel, float *yf) {
     using R = Ring<IO>;
     constexpr int kTS = R::kTS;
+    constexpr int kStages = R::kStages;
     const long long len = w.t1 - w.t0;
     if (len <= 0) return;
     const int nst = (int)((len + kTS - 1) / kTS);
@@ -431,22 +425,31 @@ __device__ __forceinline__ void sweep(const S6Params &p, WarpCtx &w, const u64 (
             // every variant does not fit the instruction cache
 #pragma unroll 1
             for (int r0 = 0; r0 < kTS; r0 += 8) {
+                // reverse half of a bidirectional output: the 8 forward halves
+                // it adds to are loaded together, ahead of the steps
+                float yfv[8];
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int r = REV ? kTS - 1 - (r0 + rr) : r0 + rr;
+                    yfv[rr] = (OUT == OUT_SUM && store) ? __ldcg(yfp + r * D) : 0.0f;
+                }
 #pragma unroll
                 for (int rr = 0; rr < 8; ++rr) {
                     const int r = REV ? kTS - 1 - (r0 + rr) : r0 + rr;
                     step<NG, LPC, IO, SP, BIDIR, MODE, OUT>(
                         to_f32(xs[r * CPW]), to_f32(ds[r * CPW]), bf + r * bstride,
                         cf + r * bstride, A2, Dd, h, hr, Q, sdel, yp + r * D,
-                        yfp ? yfp + r * D : nullptr, store);
+                        yfp ? yfp + r * D : nullptr, yfv[rr], store);
                 }
             }
         } else {
             for (int rr = 0; rr < nrows; ++rr) {
                 const int r = REV ? nrows - 1 - rr : rr;
+                const float yfv = (OUT == OUT_SUM && store) ? __ldcg(yfp + r * D) : 0.0f;
                 step<NG, LPC, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * CPW]), to_f32(ds[r * CPW]),
                                                         bf + r * bstride, cf + r * bstride, A2, Dd,
                                                         h, hr, Q, sdel, yp + r * D,
-                                                        yfp ? yfp + r * D : nullptr, store);
+                                                        yfp ? yfp + r * D : nullptr, yfv, store);
             }
         }
         __syncwarp();  // every lane is done with this slot (and the fp32 rows)
@@ -500,32 +503,63 @@ __device__ int find_anchor(const S6Params &p, long long seq, int k, unsigned tag
     }
 }
 
-// Applies the aggregates of chunks m = from, from + dir, ... (stopping before
-// `to`) to the state c, one fma per state each, in that order. The next
-// chunk's aggregate is loaded while the current one is applied, so the walk
-// costs about one L2 round trip per chunk only when it is a single chunk.
-template <int NG>
-__device__ __forceinline__ void apply_aggregates(const S6Params &p, int NF, long long seq, int from,
-                                                 int to, int dir, int fieldH, int lane,
-                                                 float (&c)[NG]) {
-    if (from == to) return;
-    float Pn[NG], Hn[NG];
-    load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + from, F_P, lane), Pn);
-    load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + from, fieldH, lane), Hn);
-    for (int m = from; m != to; m += dir) {
-        float Pm[NG], Hm[NG];
+// Chunk aggregate of this lane's states 4qd .. 4qd+3: the sub-chunk
+// aggregates (P, H) folded in sequence order, and Hr (reverse direction)
+// folded in reverse order.
+template <int NG, int NSUB, bool BIDIR>
+__device__ __forceinline__ void chunk_aggregate(const float *s_sub, int WT, int lane, int qd,
+                                                float4 &P, float4 &H, float4 &Hr) {
+    float Pv[4] = {1.0f, 1.0f, 1.0f, 1.0f}, Hv[4] = {}, Hrv[4] = {};
+    for (int v = 0; v < WT; ++v) {
+        const float *sv = s_sub + v * NSUB * NG * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < NG; ++i) {
-            Pm[i] = Pn[i];
-            Hm[i] = Hn[i];
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * qd + e;
+            Pv[e] *= sv[i * 32];
+            Hv[e] = fmaf(sv[i * 32], Hv[e], sv[(NG + i) * 32]);
         }
-        if (m + dir != to) {
-            load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m + dir, F_P, lane), Pn);
-            load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + m + dir, fieldH, lane), Hn);
-        }
-#pragma unroll
-        for (int i = 0; i < NG; ++i) c[i] = fmaf(Pm[i], c[i], Hm[i]);
     }
+    if constexpr (BIDIR) {
+        for (int v = WT - 1; v >= 0; --v) {
+            const float *sv = s_sub + v * NSUB * NG * 32 + lane;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 4 * qd + e;
+                Hrv[e] = fmaf(sv[i * 32], Hrv[e], sv[(2 * NG + i) * 32]);
+            }
+        }
+    }
+    P = make_float4(Pv[0], Pv[1], Pv[2], Pv[3]);
+    H = make_float4(Hv[0], Hv[1], Hv[2], Hv[3]);
+    Hr = make_float4(Hrv[0], Hrv[1], Hrv[2], Hrv[3]);
+}
+
+// Applies the aggregates of chunks m = from, from + dir, ... (stopping before
+// `to`) to the state quad c, one fma per state each, in that order. The
+// aggregates are loaded eight chunks at a time, so a walk over W chunks
+// waits for about W / 8 round trips to L2.
+template <int NG>
+__device__ __forceinline__ float4 apply_quads(const S6Params &p, int NF, long long seq, int from,
+                                              int to, int dir, int fieldH, int lane, int qd,
+                                              float4 c) {
+    constexpr int U = 8;
+    for (int m = from; m != to;) {
+        const int n = min(U, (to - m) * dir);
+        float4 P[U], H[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (u < n) {
+                const long long unit = seq * p.K + m + u * dir;
+                P[u] = ld_cg_f32x4(quad_ptr(field_ptr<NG>(p, NF, unit, F_P, lane), qd));
+                H[u] = ld_cg_f32x4(quad_ptr(field_ptr<NG>(p, NF, unit, fieldH, lane), qd));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (u < n) c = fma4(P[u], c, H[u]);
+        m += n * dir;
+    }
+    return c;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -537,11 +571,12 @@ s6_kernel(const __grid_constant__ S6Params p) {
     constexpr int NF = BIDIR ? 5 : 3;    // descriptor fields
     constexpr int NP = NG / 2;
     extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ int s_anchor[2];  // look-back / look-forward results
     // TMA destinations need 128-byte alignment; the launch adds 128 bytes of slack
     unsigned char *s_ring = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
-    uint64_t *s_bars = reinterpret_cast<uint64_t *>(s_ring + p.WT * Ring<IO>::kWarp);  // [WT][kStages]
-    float *s_sub = reinterpret_cast<float *>(s_bars + p.WT * kStages);      // [WT][NSUB][32][NG]
-    float *s_car = s_sub + p.WT * NSUB * 32 * NG;                           // [2][32][NG]
+    uint64_t *s_bars = reinterpret_cast<uint64_t *>(s_ring + p.WT * Ring<IO>::kWarp);  // [WT][kMaxStages]
+    float *s_sub = reinterpret_cast<float *>(s_bars + p.WT * kMaxStages);   // [WT][NSUB][32][NG]
+    float *s_car = s_sub + p.WT * NSUB * 32 * NG;  // [directions][32][NG]
 
     const bool chunked = p.K > 1;
     unsigned ticket, tag = 0;
@@ -557,7 +592,7 @@ s6_kernel(const __grid_constant__ S6Params p) {
 
     WarpCtx w;
     w.ring = s_ring + warp * Ring<IO>::kWarp;
-    w.bars = s_bars + warp * kStages;
+    w.bars = s_bars + warp * kMaxStages;
     w.slot = 0;
     w.phases = 0;
     w.lane = lane;
@@ -572,7 +607,7 @@ s6_kernel(const __grid_constant__ S6Params p) {
     w.t0 = min(tc0 + (long long)warp * p.Tsub, p.L);
     w.t1 = min(w.t0 + (long long)p.Tsub, p.L);
     if (lane == 0 && p.bulk) {
-        for (int s = 0; s < kStages; ++s) mbar_init(w.bars + s, 1);
+        for (int s = 0; s < Ring<IO>::kStages; ++s) mbar_init(w.bars + s, 1);
         fence_mbar_init();
     }
     __syncwarp();
@@ -620,84 +655,81 @@ s6_kernel(const __grid_constant__ S6Params p) {
         sweep_prime<IO, MODE_OUT, LPC, false>(p, w);
         __syncthreads();
 
-        if (warp == 0) {
-            if (chunked) {
-                // chunk aggregate: fold the sub-chunks in order
-                float Pc[NG], Hc[NG], Hrc[NG];
-#pragma unroll
-                for (int i = 0; i < NG; ++i) {
-                    Pc[i] = 1.0f;
-                    Hc[i] = 0.0f;
-                    Hrc[i] = 0.0f;
-                }
-                for (int v = 0; v < p.WT; ++v) {
-                    const float *s = s_sub + v * NSUB * NG * 32 + lane;
-#pragma unroll
-                    for (int i = 0; i < NG; ++i) {
-                        Pc[i] *= s[i * 32];
-                        Hc[i] = fmaf(s[i * 32], Hc[i], s[(NG + i) * 32]);
-                    }
-                }
-                if constexpr (BIDIR) {
-                    for (int v = p.WT - 1; v >= 0; --v) {
-                        const float *s = s_sub + v * NSUB * NG * 32 + lane;
-#pragma unroll
-                        for (int i = 0; i < NG; ++i)
-                            Hrc[i] = fmaf(s[i * 32], Hrc[i], s[(2 * NG + i) * 32]);
-                    }
-                }
-                const long long unit = seq * p.K + k;
-                store_field<NG>(field_ptr<NG>(p, NF, unit, F_P, lane), Pc);
-                store_field<NG>(field_ptr<NG>(p, NF, unit, F_H, lane), Hc);
-                if constexpr (BIDIR) store_field<NG>(field_ptr<NG>(p, NF, unit, F_HR, lane), Hrc);
-                publish_flag(p, unit, FL_AGG, tag, lane);
-
-                // forward carry: nearest inclusive state on the left, then the
-                // aggregates after it applied one by one in sequence order
-                const int j = find_anchor<true>(p, seq, k, tag, lane);
-                if (j == -2) {
-                    if (lane == 0) record_error(p.ws, SS_ERR_TIMEOUT, 3u, (unsigned)unit, 0u);
-                } else {
-                    if (j >= 0) load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + j, F_INC, lane), cf);
-                    apply_aggregates<NG>(p, NF, seq, j + 1, k, 1, F_H, lane, cf);
-                }
-                float inc[NG];
-#pragma unroll
-                for (int i = 0; i < NG; ++i) inc[i] = fmaf(Pc[i], cf[i], Hc[i]);
-                store_field<NG>(field_ptr<NG>(p, NF, unit, F_INC, lane), inc);
-                publish_flag(p, unit, FL_INC, tag, lane);
-
-                if constexpr (BIDIR) {
-                    // reverse carry: nearest reverse inclusive state on the right
-                    const int jr = find_anchor<false>(p, seq, k, tag, lane);
-                    if (jr == -2) {
-                        if (lane == 0) record_error(p.ws, SS_ERR_TIMEOUT, 4u, (unsigned)unit, 0u);
-                    } else {
-                        if (jr < p.K)
-                            load_field<NG>(field_ptr<NG>(p, NF, seq * p.K + jr, F_RINC, lane), cr);
-                        apply_aggregates<NG>(p, NF, seq, jr - 1, k, -1, F_HR, lane, cr);
-                    }
-#pragma unroll
-                    for (int i = 0; i < NG; ++i) inc[i] = fmaf(Pc[i], cr[i], Hrc[i]);
-                    store_field<NG>(field_ptr<NG>(p, NF, unit, F_RINC, lane), inc);
-                    publish_flag(p, unit, FL_RINC, tag, lane);
-                }
+        if (chunked) {
+            const long long unit = seq * p.K + k;
+            // chunk aggregate to the descriptor; the state quads of the 32
+            // channels are spread over the CTA's warps
+            for (int qd = warp; qd < NG / 4; qd += p.WT) {
+                float4 P4, H4, Hr4;
+                chunk_aggregate<NG, NSUB, BIDIR>(s_sub, p.WT, lane, qd, P4, H4, Hr4);
+                __stcg(quad_ptr(field_ptr<NG>(p, NF, unit, F_P, lane), qd), P4);
+                __stcg(quad_ptr(field_ptr<NG>(p, NF, unit, F_H, lane), qd), H4);
+                if constexpr (BIDIR) __stcg(quad_ptr(field_ptr<NG>(p, NF, unit, F_HR, lane), qd), Hr4);
             }
+            publish_cta(p, unit, FL_AGG, tag);
+            // nearest published inclusive state on the left
+            if (warp == 0) {
+                const int j = find_anchor<true>(p, seq, k, tag, lane);
+                if (lane == 0) s_anchor[0] = j;
+            }
+            __syncthreads();
+
+            // forward carry: the anchor's inclusive state, then the aggregates
+            // after it applied in sequence order
+            const int j = s_anchor[0];
+            if (j == -2 && threadIdx.x == 0) record_error(p.ws, SS_ERR_TIMEOUT, 3u, (unsigned)unit, 0u);
+            for (int qd = warp; qd < NG / 4; qd += p.WT) {
+                float4 c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (j >= 0) c = ld_cg_f32x4(quad_ptr(field_ptr<NG>(p, NF, seq * p.K + j, F_INC, lane), qd));
+                if (j != -2) c = apply_quads<NG>(p, NF, seq, j + 1, k, 1, F_H, lane, qd, c);
+                s_car[(4 * qd) * 32 + lane] = c.x;
+                s_car[(4 * qd + 1) * 32 + lane] = c.y;
+                s_car[(4 * qd + 2) * 32 + lane] = c.z;
+                s_car[(4 * qd + 3) * 32 + lane] = c.w;
+                float4 P4, H4, Hr4;
+                chunk_aggregate<NG, NSUB, BIDIR>(s_sub, p.WT, lane, qd, P4, H4, Hr4);
+                __stcg(quad_ptr(field_ptr<NG>(p, NF, unit, F_INC, lane), qd), fma4(P4, c, H4));
+            }
+            publish_cta(p, unit, FL_INC, tag);
+
+            if constexpr (BIDIR) {
+                // reverse carry: the same on the right, in reverse order. The
+                // search starts only after this chunk's forward inclusive state
+                // is out: a forward walk never waits on a reverse one, so the
+                // two chains cannot wait on each other.
+                if (warp == 0) {
+                    const int jr0 = find_anchor<false>(p, seq, k, tag, lane);
+                    if (lane == 0) s_anchor[1] = jr0;
+                }
+                __syncthreads();
+                const int jr = s_anchor[1];
+                if (jr == -2 && threadIdx.x == 0) record_error(p.ws, SS_ERR_TIMEOUT, 4u, (unsigned)unit, 0u);
+                for (int qd = warp; qd < NG / 4; qd += p.WT) {
+                    float4 c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (jr >= 0 && jr < p.K)
+                        c = ld_cg_f32x4(quad_ptr(field_ptr<NG>(p, NF, seq * p.K + jr, F_RINC, lane), qd));
+                    if (jr != -2) c = apply_quads<NG>(p, NF, seq, jr - 1, k, -1, F_HR, lane, qd, c);
+                    s_car[(NG + 4 * qd) * 32 + lane] = c.x;
+                    s_car[(NG + 4 * qd + 1) * 32 + lane] = c.y;
+                    s_car[(NG + 4 * qd + 2) * 32 + lane] = c.z;
+                    s_car[(NG + 4 * qd + 3) * 32 + lane] = c.w;
+                    float4 P4, H4, Hr4;
+                    chunk_aggregate<NG, NSUB, BIDIR>(s_sub, p.WT, lane, qd, P4, H4, Hr4);
+                    __stcg(quad_ptr(field_ptr<NG>(p, NF, unit, F_RINC, lane), qd), fma4(P4, c, Hr4));
+                }
+                publish_cta(p, unit, FL_RINC, tag);
+            }
+            // (the barrier in publish_cta also completes s_car)
 #pragma unroll
             for (int i = 0; i < NG; ++i) {
-                s_car[i * 32 + lane] = cf[i];
-                s_car[(NG + i) * 32 + lane] = cr[i];
+                cf[i] = s_car[i * 32 + lane];
+                if constexpr (BIDIR) cr[i] = s_car[(NG + i) * 32 + lane];
             }
         }
-        __syncthreads();
 
-        // this warp's carries: the chunk carry moved across the earlier
-        // (forward) or later (reverse) sub-chunks of the CTA, in order
-#pragma unroll
-        for (int i = 0; i < NG; ++i) {
-            cf[i] = s_car[i * 32 + lane];
-            cr[i] = s_car[(NG + i) * 32 + lane];
-        }
+        // this warp's carries: the chunk carry (zero for an unsplit
+        // sequence) moved across the earlier (forward) or later (reverse)
+        // sub-chunks of the CTA, in order
         for (int v = 0; v < warp; ++v) {
             const float *s = s_sub + v * NSUB * NG * 32 + lane;
 #pragma unroll
@@ -808,8 +840,8 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     pl.total = 0;
     if (pl.K > 1 || pl.scratch_bytes) pl.total = kWsHeaderBytes + pl.desc_bytes + pl.scratch_bytes;
     const size_t ring = io_bf16 ? Ring<__nv_bfloat16>::kWarp : Ring<float>::kWarp;
-    pl.smem = 128 + (size_t)pl.WT * (ring + kStages * sizeof(uint64_t)) +
-              (size_t)(pl.WT * NSUB + 2) * 32 * pl.NG * sizeof(float);
+    pl.smem = 128 + (size_t)pl.WT * (ring + kMaxStages * sizeof(uint64_t)) +
+              (size_t)(pl.WT * NSUB + (bidir ? 2 : 1)) * 32 * pl.NG * sizeof(float);
     return pl;
 }
 

@@ -39,11 +39,21 @@ def plan_override():
 
 
 def gpu_run(ss, torch, inp, softplus, bidir):
+    """Runs the scan on a fresh workspace and checks that the device reported
+    no error (a look-back that ran out of time would otherwise only show up
+    as wrong numbers)."""
     dev = torch.device("cuda:0")
     t = lambda v: to_dev(v, dev, inp.io)
     fn = ss.ss_selective_scan_bidir if bidir else ss.ss_selective_scan_fwd
+    B, L, D = inp.x.shape
+    N = inp.Bt.shape[-1]
+    io = ss.SS_BF16 if inp.io == "bf16" else ss.SS_F32
+    nbytes = ss.ss_selective_scan_workspace_bytes(B, L, D, N, io, bidir)
+    ws = ss.new_workspace(nbytes, dev) if nbytes else None
     y = fn(t(inp.x), t(inp.delta), t(inp.Bt), t(inp.Ct), t(inp.A), t(inp.Dskip),
-           delta_softplus=softplus)
+           delta_softplus=softplus, workspace=ws)
+    if ws is not None:
+        assert ss.ss_get_device_status(ws) == ss.SS_OK
     return to_host_f64(y)
 
 
@@ -92,6 +102,17 @@ def test_chunk_splits(torch, ss, plan_override, wt, tsub, bidir):
     and the in-CTA folds run across ragged boundaries."""
     plan_override(wt, tsub)
     inp = small(2, 777, 70, 16, seed=wt * 100 + tsub)
+    y = gpu_run(ss, torch, inp, False, bidir)
+    assert rel_err(y, oracle_run(inp, False, bidir)) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
+def test_more_chunks_than_one_lookback_window(torch, ss, plan_override, bidir):
+    """300 chunks: walks reach past the 128 chunks a look-back examines at
+    once, in both directions, and the two directions must not wait on each
+    other."""
+    plan_override(1, 2)
+    inp = small(1, 600, 40, 16, seed=77)
     y = gpu_run(ss, torch, inp, False, bidir)
     assert rel_err(y, oracle_run(inp, False, bidir)) <= TOL["f32"]
 
