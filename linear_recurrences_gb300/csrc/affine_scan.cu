@@ -8,6 +8,9 @@
 //
 //  * a persistent grid (as many CTAs as fit) takes 4096-element tiles from a
 //    ticket counter in start order, so every lower tile is running or done;
+//    a CTA asks L2 to prefetch each tile when it takes the tile's ticket, a
+//    step before the tile is staged into shared memory (prefetching further
+//    ahead, or holding tickets further ahead, measured slower);
 //  * each CTA owns a ring of kBufs tile buffers in shared memory, filled by
 //    two bulk async copies (cp.async.bulk) per tile on an mbarrier, 8 compute
 //    warps and one control warp. Per step the compute warps scan the next
@@ -33,8 +36,8 @@
 // matter which earlier tile the walk started from, so e_k == I_{k-1} always
 // and every output is independent of scheduling.
 //
-// Progress: a CTA holds at most kBufs + 1 tickets (current and the ones after it),
-// scanned and published in ticket order. The lowest unfinished tile is
+// Progress: a CTA holds at most kTicks + 1 tickets (current and the ones after
+// it), scanned and published in ticket order. The lowest unfinished tile is
 // always some CTA's current tile and every tile below it is finished, so its
 // look-back completes.
 #include <algorithm>
@@ -55,6 +58,7 @@ constexpr int kWarpElems = 32 * kItems;    // 512 elements per warp
 constexpr int kMaxWindows = 8;             // look-back holds up to 256 predecessors
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBufs = 2;                                     // tile buffers per CTA
+constexpr int kTicks = kBufs;  // tickets a CTA holds: one per buffer
 constexpr size_t kDynSmem = 2 * kBufs * kTile * sizeof(float);  // a and b per buffer
 constexpr unsigned long long kCopyTimeoutNs = 2000000000ull;  // bulk-copy completion bound
 
@@ -122,6 +126,18 @@ __device__ __forceinline__ void stage_tile(const AffineParams &p, unsigned tile,
             sa[i] = in ? p.a[base + i] : 1.0f;
             sb[i] = in ? p.b[base + i] : 0.0f;
         }
+    }
+}
+
+// Asks L2 to fetch tile `tile`'s inputs ahead of its staging (full tiles of
+// aligned inputs only; the hint changes no data).
+__device__ __forceinline__ void prefetch_tile_l2(const AffineParams &p, long long tile) {
+    const long long base = tile * kTile;
+    if (p.bulk_ok && p.n - base >= kTile) {
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     :: "l"(p.a + base), "r"((unsigned)(kTile * sizeof(float))) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     :: "l"(p.b + base), "r"((unsigned)(kTile * sizeof(float))) : "memory");
     }
 }
 
@@ -220,14 +236,15 @@ __device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, 
                 const TileDesc *d = p.desc + t;
                 kind = 0;
                 for (unsigned it = 0;; ++it) {
+                    // all three words in one round trip
                     const unsigned long long wi = ld_relaxed_u64(&d->inc);
+                    const unsigned long long wa = ld_relaxed_u64(&d->agg_a);
+                    const unsigned long long wb = ld_relaxed_u64(&d->agg_b);
                     if (tag_of(wi) == tag) {
                         v = val_of(wi);
                         kind = 2;
                         break;
                     }
-                    const unsigned long long wa = ld_relaxed_u64(&d->agg_a);
-                    const unsigned long long wb = ld_relaxed_u64(&d->agg_b);
                     if (tag_of(wa) == tag && tag_of(wb) == tag) {
                         g = {val_of(wa), val_of(wb)};
                         kind = 1;
@@ -336,13 +353,14 @@ struct AffineShared {
     uint64_t bar[kBufs];       // one mbarrier per tile buffer
     Pair warp_agg[kWarps];     // per-warp aggregates of the tile being scanned
     Pair tagg[2];              // tile aggregates handed to the control warp
-    unsigned tick[kBufs];      // tickets of the tiles staged or about to be
+    unsigned tick[kTicks];     // ticket of CTA-local tile q in tick[q % kTicks]
     unsigned tag;              // this launch's descriptor tag
     float carry;               // state entering the current tile
 };
 
-// Control warp: per step, take the ticket of tile q + kBufs, look back for
-// tile q, then meet the compute warps at the step's two barriers.
+// Control warp: per step, take the ticket of tile q + kTicks (and prefetch it
+// to L2), look back for tile q, then meet the compute warps at the step's two
+// barriers.
 __device__ __forceinline__ void control_loop(const AffineParams &p, AffineShared &sh, Pair *s_walk,
                                              unsigned num_tiles) {
     const int lane = threadIdx.x & 31;
@@ -352,13 +370,16 @@ __device__ __forceinline__ void control_loop(const AffineParams &p, AffineShared
     for (unsigned q = 0; cur < num_tiles; ++q) {
         // ticket first: its round trip overlaps the look-back's polls
         unsigned t = 0;
-        if (lane == 0) t = atomicAdd(&p.ws->ticket, 1u);
+        if (lane == 0) {
+            t = atomicAdd(&p.ws->ticket, 1u);
+            if (t < num_tiles) prefetch_tile_l2(p, t);  // staged at the end of this step
+        }
         look_back(p, cur, tag, sh.tagg[q & 1], s_walk, &sh.carry);
-        if (lane == 0) sh.tick[q % kBufs] = t;
+        if (lane == 0) sh.tick[q % kTicks] = t;  // tile q's slot is no longer read
         __syncthreads();  // carry and ticket are published
         __syncthreads();  // tile q is stored, its buffer restaged
         cur = nxt;
-        nxt = sh.tick[(q + 2) % kBufs];
+        nxt = sh.tick[(q + 2) % kTicks];
     }
 }
 
@@ -384,13 +405,13 @@ __device__ __forceinline__ void compute_loop(const AffineParams &p, AffineShared
             scan_tile(p, nxt, tag, abuf(q + 1), abuf(q + 1) + kTile, &sh.bar[(q + 1) % kBufs],
                       (q + 1) / kBufs, sh.warp_agg, &sh.tagg[1], rn);
         __syncthreads();
-        unsigned after = sh.tick[q % kBufs];
+        unsigned after = sh.tick[(q + kBufs) % kTicks];
         fix_up(p, cur, abuf(q), abuf(q) + kTile, rc, sh.carry);
         compute_sync();  // tile q's buffer is free
         if (after < num_tiles) stage_tile(p, after, abuf(q), abuf(q) + kTile, &sh.bar[q % kBufs]);
         __syncthreads();
         cur = nxt;
-        nxt = sh.tick[(q + 2) % kBufs];
+        nxt = sh.tick[(q + 2) % kTicks];
         if (cur >= num_tiles) break;
 
         const unsigned q1 = q + 1;
@@ -398,13 +419,13 @@ __device__ __forceinline__ void compute_loop(const AffineParams &p, AffineShared
             scan_tile(p, nxt, tag, abuf(q1 + 1), abuf(q1 + 1) + kTile, &sh.bar[(q1 + 1) % kBufs],
                       (q1 + 1) / kBufs, sh.warp_agg, &sh.tagg[0], rc);
         __syncthreads();
-        after = sh.tick[q1 % kBufs];
+        after = sh.tick[(q1 + kBufs) % kTicks];
         fix_up(p, cur, abuf(q1), abuf(q1) + kTile, rn, sh.carry);
         compute_sync();
         if (after < num_tiles) stage_tile(p, after, abuf(q1), abuf(q1) + kTile, &sh.bar[q1 % kBufs]);
         __syncthreads();
         cur = nxt;
-        nxt = sh.tick[(q1 + 2) % kBufs];
+        nxt = sh.tick[(q1 + 2) % kTicks];
     }
 }
 
@@ -426,10 +447,8 @@ affine_scan_kernel(const AffineParams p) {
     const unsigned num_tiles = (unsigned)((p.n + kTile - 1) / kTile);
     if (threadIdx.x == kThreads) {
         sh.tag = ld_relaxed_u32(&p.ws->epoch) + 1u;
-        for (int i = 0; i < kBufs; ++i) {
-            sh.tick[i] = atomicAdd(&p.ws->ticket, 1u);
-            mbar_init(&sh.bar[i], 1);
-        }
+        for (int i = 0; i < kTicks; ++i) sh.tick[i] = atomicAdd(&p.ws->ticket, 1u);
+        for (int i = 0; i < kBufs; ++i) mbar_init(&sh.bar[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
