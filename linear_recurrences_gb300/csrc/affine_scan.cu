@@ -23,9 +23,10 @@
 //    four interleaved warp-shuffle scans and a fold over the 8 warps give
 //    the tile aggregate;
 //  * the aggregate is published as two tagged 64-bit words; the control warp
-//    walks back 32 predecessors at a time to the nearest tile that has
-//    published its inclusive state, and lane 0 applies the aggregates after
-//    it to that state one by one, in sequence order;
+//    walks back 64 predecessors per L2 round trip (each lane loads all three
+//    words of two tiles at once) to the nearest tile that has published its
+//    inclusive state, and lane 0 applies the aggregates after it to that
+//    state one by one, in sequence order;
 //  * the tile's inclusive state is published, and each lane re-sweeps its
 //    elements from shared memory starting at its carry-in, storing h with
 //    coalesced 128-bit streaming stores.
@@ -56,6 +57,8 @@ constexpr int kTile = kThreads * kItems;   // 4096 elements per tile
 constexpr int kStripes = kItems / 4;       // float4 slices per thread
 constexpr int kWarpElems = 32 * kItems;    // 512 elements per warp
 constexpr int kMaxWindows = 8;             // look-back holds up to 256 predecessors
+constexpr int kPoll = 2;                   // windows polled per round trip
+static_assert(kMaxWindows % kPoll == 0, "windows are polled kPoll at a time");
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kBufs = 2;                                     // tile buffers per CTA
 constexpr int kTicks = kBufs;  // tickets a CTA holds: one per buffer
@@ -228,51 +231,78 @@ __device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, 
         bool timed_out = false;
         const uint64_t walk_t0 = globaltimer_ns();
         for (;;) {
-            const long long t = (long long)tile - 32LL * (win + 1) + lane;
-            int kind = 2;  // before tile 0: the state h[-1] = 0 counts as inclusive
-            float v = 0.0f;
-            Pair g = {1.0f, 0.0f};
-            if (t >= 0) {
-                const TileDesc *d = p.desc + t;
-                kind = 0;
-                for (unsigned it = 0;; ++it) {
-                    // all three words in one round trip
-                    const unsigned long long wi = ld_relaxed_u64(&d->inc);
-                    const unsigned long long wa = ld_relaxed_u64(&d->agg_a);
-                    const unsigned long long wb = ld_relaxed_u64(&d->agg_b);
-                    if (tag_of(wi) == tag) {
-                        v = val_of(wi);
-                        kind = 2;
-                        break;
-                    }
-                    if (tag_of(wa) == tag && tag_of(wb) == tag) {
-                        g = {val_of(wa), val_of(wb)};
-                        kind = 1;
-                        break;
-                    }
-                    if ((it & 63u) == 63u &&
-                        (globaltimer_ns() - walk_t0 > p.timeout_ns || ld_relaxed_u32(&p.ws->error) != 0u))
-                        break;  // kind stays 0: gave up
-                }
+            // kPoll windows per round trip: lane l polls tiles
+            // tile - 32(win + 1 + i) + l, i < kPoll
+            int kind[kPoll];  // 0 nothing yet, 1 aggregate, 2 inclusive state
+            float v[kPoll];
+            Pair g[kPoll];
+#pragma unroll
+            for (int i = 0; i < kPoll; ++i) {
+                // before tile 0: the state h[-1] = 0 counts as inclusive
+                kind[i] = (long long)tile - 32LL * (win + 1 + i) + lane < 0 ? 2 : 0;
+                v[i] = 0.0f;
+                g[i] = {1.0f, 0.0f};
             }
-            s_walk[win * 32 + lane] = g;
-            if (__ballot_sync(kFull, kind == 0)) {
+            for (unsigned it = 0;; ++it) {
+                unsigned long long wi[kPoll], wa[kPoll], wb[kPoll];
+#pragma unroll
+                for (int i = 0; i < kPoll; ++i) {  // every word in flight at once
+                    if (kind[i] == 0) {
+                        const TileDesc *d = p.desc + (tile - 32LL * (win + 1 + i) + lane);
+                        wi[i] = ld_relaxed_u64(&d->inc);
+                        wa[i] = ld_relaxed_u64(&d->agg_a);
+                        wb[i] = ld_relaxed_u64(&d->agg_b);
+                    }
+                }
+                bool pending = false;
+#pragma unroll
+                for (int i = 0; i < kPoll; ++i) {
+                    if (kind[i] == 0) {
+                        if (tag_of(wi[i]) == tag) {
+                            v[i] = val_of(wi[i]);
+                            kind[i] = 2;
+                        } else if (tag_of(wa[i]) == tag && tag_of(wb[i]) == tag) {
+                            g[i] = {val_of(wa[i]), val_of(wb[i])};
+                            kind[i] = 1;
+                        } else {
+                            pending = true;
+                        }
+                    }
+                }
+                if (!pending) break;
+                if ((it & 63u) == 63u &&
+                    (globaltimer_ns() - walk_t0 > p.timeout_ns || ld_relaxed_u32(&p.ws->error) != 0u))
+                    break;  // a kind stays 0: gave up
+            }
+            bool gave_up = false;
+#pragma unroll
+            for (int i = 0; i < kPoll; ++i) {
+                s_walk[(win + i) * 32 + lane] = g[i];
+                gave_up |= kind[i] == 0;
+            }
+            if (__ballot_sync(kFull, gave_up)) {
                 timed_out = true;
                 break;
             }
-            const unsigned incs = __ballot_sync(kFull, kind == 2);
-            if (incs) {
-                anchor_lane = 31 - __clz(incs);
-                anchor = __shfl_sync(kFull, v, anchor_lane);
-                break;
+            bool found = false;
+#pragma unroll
+            for (int i = 0; i < kPoll; ++i) {
+                const unsigned incs = __ballot_sync(kFull, kind[i] == 2);
+                if (!found && incs) {  // nearest window holding an inclusive state
+                    win += i;
+                    anchor_lane = 31 - __clz(incs);
+                    anchor = __shfl_sync(kFull, v[i], anchor_lane);
+                    found = true;
+                }
             }
-            if (win + 1 < kMaxWindows) {
-                ++win;
+            if (found) break;
+            if (win + kPoll < kMaxWindows) {
+                win += kPoll;
             } else if (globaltimer_ns() - walk_t0 > p.timeout_ns ||
                        ld_relaxed_u32(&p.ws->error) != 0u) {
-                timed_out = true;  // oldest window never showed an inclusive state
+                timed_out = true;  // oldest windows never showed an inclusive state
                 break;
-            }  // else poll the oldest window again
+            }  // else poll the oldest windows again
         }
         __syncwarp();
         if (timed_out) {
