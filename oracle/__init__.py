@@ -66,6 +66,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_s6_fwd_f64.restype = ctypes.c_int
     lib.oracle_s6_bidir_f64.argtypes = s6
     lib.oracle_s6_bidir_f64.restype = ctypes.c_int
+    lib.oracle_s6_fwd_state_f64.argtypes = [f, f, f, f, f, f, dp, dp, dp, i64, i64, i64, i64,
+                                            ctypes.c_int, ctypes.c_int]
+    lib.oracle_s6_fwd_state_f64.restype = ctypes.c_int
     lib.oracle_s6_channels_f64.argtypes = [
         f, f, f, f, f, f, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
         ctypes.POINTER(ctypes.c_int64), i64, dp, ctypes.c_int]
@@ -127,6 +130,28 @@ def s6_fwd(x, delta, Bt, Ct, A, Dskip=None, softplus=False, threads=1,
     if rc:
         raise RuntimeError(f"oracle_s6_fwd_f64 failed ({rc})")
     return y
+
+
+def s6_fwd_state(x, delta, Bt, Ct, A, Dskip=None, h0=None, softplus=False, threads=1,
+                 lib: ctypes.CDLL | None = None):
+    """S6 forward from the state h0 ((B, D, N), zeros if None); returns
+    (y (B, L, D), h_last (B, D, N)) in float64."""
+    lib = lib or load()
+    x, delta, Bt, Ct, A, Dskip, B, L, D, N = _s6_args(x, delta, Bt, Ct, A, Dskip)
+    h0p = None
+    if h0 is not None:
+        h0 = np.ascontiguousarray(h0, dtype=np.float64)
+        if h0.shape != (B, D, N):
+            raise ValueError("h0 must be (B, D, N)")
+        h0p = _p(h0, ctypes.c_double)
+    y = np.zeros((B, L, D), dtype=np.float64)
+    h_last = np.zeros((B, D, N), dtype=np.float64)
+    rc = lib.oracle_s6_fwd_state_f64(_p(x), _p(delta), _p(Bt), _p(Ct), _p(A), _p(Dskip), h0p,
+                                     _p(y, ctypes.c_double), _p(h_last, ctypes.c_double),
+                                     B, L, D, N, int(bool(softplus)), int(threads))
+    if rc:
+        raise RuntimeError(f"oracle_s6_fwd_state_f64 failed ({rc})")
+    return y, h_last
 
 
 def s6_bidir(x, delta, Bt, Ct, A, Dskip=None, softplus=False, threads=1,

@@ -31,6 +31,10 @@
  *     h_rev[t] = dA[t]*h_rev[t+1] + dBx[t], i.e. the forward scan of the
  *     time-reversed inputs, read back in original order.
  *   - in the bidirectional output each direction carries its own D*x term.
+ *   - state in/out (forward only): h0 (B, D, N) replaces the zero state
+ *     before t = 0, and h_last (B, D, N) is the state after t = L-1; running
+ *     [0, L1) and then [L1, L) from the first run's h_last is the same loop
+ *     as running [0, L) in one go.
  */
 #include <math.h>
 #include <pthread.h>
@@ -66,6 +70,8 @@ typedef struct {
     int bidir;
     const int64_t *chans;   /* channel c = b*D + d; NULL means all B*D */
     int64_t nchan;
+    const double *h0;       /* (B, D, N) state before t = 0; NULL: zeros */
+    double *hlast;          /* (B, D, N) state after t = L-1; NULL: not kept */
     double *out;            /* chans != NULL: (nchan, L); else (B, L, D) */
     int64_t begin, end;     /* range of channel slots this worker owns */
 } s6_job;
@@ -79,9 +85,9 @@ static void s6_channel(const s6_job *j, int64_t b, int64_t d, double *h,
     const int64_t L = j->L, D = j->D, N = j->N;
     const double Dd = (double)j->Dskip[d];
 
-    /* forward: t = 0 .. L-1 */
+    /* forward: t = 0 .. L-1, from h0 (zeros unless given) */
     for (int64_t n = 0; n < N; ++n)
-        h[n] = 0.0;
+        h[n] = j->h0 ? j->h0[(b * D + d) * N + n] : 0.0;
     for (int64_t t = 0; t < L; ++t) {
         const int64_t xi = (b * L + t) * D + d;   /* x[b, t, d] */
         const int64_t bi = (b * L + t) * N;       /* B_t[b, t, :] */
@@ -99,6 +105,9 @@ static void s6_channel(const s6_job *j, int64_t b, int64_t d, double *h,
         }
         y[t * ystride] = acc + xv * Dd;
     }
+    if (j->hlast)
+        for (int64_t n = 0; n < N; ++n)
+            j->hlast[(b * D + d) * N + n] = h[n];
     if (!j->bidir)
         return;
 
@@ -194,7 +203,21 @@ int oracle_s6_fwd_f64(const float *x, const float *delta, const float *Bt,
                       int softplus, int threads)
 {
     s6_job j = {x, delta, Bt, Ct, A, Dskip, B, L, D, N, softplus, 0,
-                NULL, 0, y, 0, 0};
+                NULL, 0, NULL, NULL, y, 0, 0};
+    return s6_run(j, threads);
+}
+
+/* [S6] forward pass from the state h0 (NULL: zeros), also returning the
+ * state after the last step in h_last (NULL: not returned); h0 and h_last
+ * are (B, D, N) float64, y is (B, L, D). */
+int oracle_s6_fwd_state_f64(const float *x, const float *delta, const float *Bt,
+                            const float *Ct, const float *A, const float *Dskip,
+                            const double *h0, double *y, double *h_last,
+                            int64_t B, int64_t L, int64_t D, int64_t N,
+                            int softplus, int threads)
+{
+    s6_job j = {x, delta, Bt, Ct, A, Dskip, B, L, D, N, softplus, 0,
+                NULL, 0, h0, h_last, y, 0, 0};
     return s6_run(j, threads);
 }
 
@@ -205,7 +228,7 @@ int oracle_s6_bidir_f64(const float *x, const float *delta, const float *Bt,
                         int softplus, int threads)
 {
     s6_job j = {x, delta, Bt, Ct, A, Dskip, B, L, D, N, softplus, 1,
-                NULL, 0, y, 0, 0};
+                NULL, 0, NULL, NULL, y, 0, 0};
     return s6_run(j, threads);
 }
 
@@ -221,6 +244,6 @@ int oracle_s6_channels_f64(const float *x, const float *delta, const float *Bt,
         if (chans[i] < 0 || chans[i] >= B * D)
             return -2;
     s6_job j = {x, delta, Bt, Ct, A, Dskip, B, L, D, N, softplus, bidir,
-                chans, nchan, out, 0, 0};
+                chans, nchan, NULL, NULL, out, 0, 0};
     return s6_run(j, threads);
 }

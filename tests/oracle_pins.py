@@ -25,6 +25,10 @@ What pins what:
           time-reversal involution of the bidirectional output; bidir equals
           forward plus flipped forward of flipped inputs; linearity in x;
           channel permutation equivariance; batch independence.
+  state   forward from an initial state h0: the matrix form plus h0's decay
+          term, and the final state's matrix form; x == 0: pure decay of h0
+          in closed form; a run split at any step and resumed from the first
+          part's final state equals the unsplit run exactly.
 """
 from __future__ import annotations
 
@@ -312,9 +316,72 @@ def pin_s6_channel_structure(lib):
         assert np.array_equal(yc[i], y[c // 5, :, c % 5]), "channel sampler agrees"
 
 
+def _state_matrix_form(x, dl, Bt, Ct, A, Ds, h0):
+    """The forward matrix form plus the initial state's response
+    y[t] += sum_n C[t,n] exp(A[d,n] sum_{i<=t} delta_i) h0[n], and the final
+    state h_last[n] = sum_j exp(A[d,n] sum_{i=j+1..L-1} delta_i) delta_j B[j,n]
+    x_j + exp(A[d,n] sum_i delta_i) h0[n]."""
+    y = _matrix_form(x, dl, Bt, Ct, A, Ds, softplus=False, bidir=False)
+    B, L, D = x.shape
+    N = A.shape[1]
+    hl = np.zeros((B, D, N))
+    for b in range(B):
+        for d in range(D):
+            dd = [float(dl[b, t, d]) for t in range(L)]
+            for t in range(L):
+                s = math.fsum(dd[: t + 1])
+                y[b, t, d] += math.fsum(float(Ct[b, t, n]) * math.exp(float(A[d, n]) * s)
+                                        * float(h0[b, d, n]) for n in range(N))
+            for n in range(N):
+                terms = [math.exp(float(A[d, n]) * math.fsum(dd[j + 1:])) * dd[j]
+                         * float(Bt[b, j, n]) * float(x[b, j, d]) for j in range(L)]
+                terms.append(math.exp(float(A[d, n]) * math.fsum(dd)) * float(h0[b, d, n]))
+                hl[b, d, n] = math.fsum(terms)
+    return y, hl
+
+
+def pin_s6_state_matrix_form(lib):
+    args = _small_s6(21, L=10)
+    h0 = _rng(22).standard_normal((2, 3, 4))
+    y, hl = oracle.s6_fwd_state(*args, h0=h0, lib=lib)
+    ry, rhl = _state_matrix_form(*args, h0)
+    assert _rel(y, ry) < 1e-12, "forward from h0: matrix form"
+    assert _rel(hl, rhl) < 1e-12, "final state: matrix form"
+
+
+def pin_s6_state_x_zero(lib):
+    x, dl, Bt, Ct, A, Ds = _small_s6(23, L=40)
+    h0 = _rng(24).standard_normal((2, 3, 4))
+    y, hl = oracle.s6_fwd_state(np.zeros_like(x), dl, Bt, Ct, A, Ds, h0=h0, lib=lib)
+    # no input: h[t, n] = exp(A[d, n] * sum_{i<=t} delta_i) * h0[n]
+    S = np.cumsum(dl.astype(np.float64), axis=1)                       # (B, L, D)
+    h = np.exp(S[:, :, :, None] * A.astype(np.float64)[None, None]) * h0[:, None]
+    assert _rel(y, np.einsum("bldn,bln->bld", h, Ct.astype(np.float64))) < 1e-12, \
+        "x == 0: decay of h0"
+    assert _rel(hl, h[:, -1]) < 1e-12, "x == 0: final state"
+
+
+def pin_s6_state_split(lib):
+    args = _small_s6(25, L=31)
+    x, dl, Bt, Ct, A, Ds = args
+    h0 = _rng(26).standard_normal((2, 3, 4))
+    y, hl = oracle.s6_fwd_state(*args, h0=h0, lib=lib)
+    cut = lambda v, a, b: np.ascontiguousarray(v[:, a:b])
+    for L1 in (1, 12, 30):
+        y1, h1 = oracle.s6_fwd_state(cut(x, 0, L1), cut(dl, 0, L1), cut(Bt, 0, L1),
+                                     cut(Ct, 0, L1), A, Ds, h0=h0, lib=lib)
+        y2, h2 = oracle.s6_fwd_state(cut(x, L1, 31), cut(dl, L1, 31), cut(Bt, L1, 31),
+                                     cut(Ct, L1, 31), A, Ds, h0=h1, lib=lib)
+        assert np.array_equal(np.concatenate([y1, y2], axis=1), y), "split run == one run"
+        assert np.array_equal(h2, hl), "split run's final state == one run's"
+    y0, _ = oracle.s6_fwd_state(*args, lib=lib)
+    assert np.array_equal(y0, oracle.s6_fwd(*args, lib=lib)), "h0 = None is the zero state"
+
+
 S6_PINS = [pin_s6_matrix_form, pin_s6_bidir_matrix_form, pin_s6_A_zero,
            pin_s6_C_zero_and_delta_zero, pin_s6_one_step, pin_softplus,
-           pin_s6_reversal, pin_s6_linear_in_x, pin_s6_channel_structure]
+           pin_s6_reversal, pin_s6_linear_in_x, pin_s6_channel_structure,
+           pin_s6_state_matrix_form, pin_s6_state_x_zero, pin_s6_state_split]
 
 ALL_PINS = AFFINE_PINS + S6_PINS
 

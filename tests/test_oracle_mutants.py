@@ -45,6 +45,14 @@ MUTANTS = [
      "for (int64_t t = L - 1; t >= 0; --t)", "for (int64_t t = 0; t < L; ++t)", 1),
     ("bidir_reverse_drops_skip_term",
      "y[t * ystride] += acc + xv * Dd;", "y[t * ystride] += acc;", 1),
+    ("state_h0_ignored",
+     "h[n] = j->h0 ? j->h0[(b * D + d) * N + n] : 0.0;", "h[n] = 0.0;", 1),
+    ("state_h0_index_transposed",
+     "h[n] = j->h0 ? j->h0[(b * D + d) * N + n] : 0.0;",
+     "h[n] = j->h0 ? j->h0[(b * N + n) * D + d] : 0.0;", 1),
+    ("state_hlast_is_h0",
+     "j->hlast[(b * D + d) * N + n] = h[n];",
+     "j->hlast[(b * D + d) * N + n] = j->h0 ? j->h0[(b * D + d) * N + n] : 0.0;", 1),
     ("bidir_reverse_state_not_reset",
      "    /* reverse: t = L-1 .. 0, h_rev[t] = dA[t]*h_rev[t+1] + dBx[t] */\n"
      "    for (int64_t n = 0; n < N; ++n)\n        h[n] = 0.0;\n",
