@@ -226,8 +226,13 @@ def s6_bytes_and_ops(w):
 
 
 def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
+    """One S6 workload; a name ending in "_state" runs the forward-with-state
+    call on the workload before the suffix, from a seeded random h0 and
+    writing h_last (2 x B*D*N*4 more bytes)."""
+    import numpy as np
     import workloads
-    w = workloads.S6[name]
+    state = name.endswith("_state")
+    w = workloads.S6[name[: -len("_state")] if state else name]
     inp = workloads.s6_workload_inputs(w)
 
     def t(v):
@@ -241,6 +246,13 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
     fn = ss.ss_selective_scan_bidir if w.bidir else ss.ss_selective_scan_fwd
     call = lambda: fn(*args, delta_softplus=w.softplus, y=y, stream=stream)
     byts, mufu = s6_bytes_and_ops(w)
+    if state:
+        g = np.random.Generator(np.random.PCG64(7))
+        h0 = torch.from_numpy(g.standard_normal((w.B, w.D, w.N)).astype(np.float32)).to(dev)
+        h_last = torch.empty_like(h0)
+        call = lambda: ss.ss_selective_scan_fwd_state(*args, h0=h0, delta_softplus=w.softplus,
+                                                      y=y, h_last=h_last, stream=stream)
+        byts += 2 * 4 * w.B * w.D * w.N
     flush = None
     if byts < 2 * L2_BYTES:
         junk = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -252,7 +264,7 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
     t_roof = max(t_hbm, t_sfu)
     return {
         "elements": w.elements, "shape": [w.B, w.L, w.D, w.N], "io": w.io,
-        "softplus": w.softplus, "bidir": w.bidir, "ms": ms, "ms_min": min(per),
+        "softplus": w.softplus, "bidir": w.bidir, "state": state, "ms": ms, "ms_min": min(per),
         "elements_per_s": w.elements / (ms * 1e-3),
         "gbs": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts, "mufu_ops": mufu,
         "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6,
@@ -393,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
         per_cfg[HEADLINE] = {"elements": w.n, "ms": launch_ms,
                              "elements_per_s": w.n / (launch_ms * 1e-3), "gbs": achieved,
                              "bound": "hbm", "roofline_frac": achieved / hbm_peak}
-        for name in ("s6_fp32", "s6_bf16", "s6_bidir"):
+        for name in ("s6_fp32", "s6_bf16", "s6_bidir", "s6_bf16_state"):
             per_cfg[name] = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream,
                                      hbm_peak, sfu)
         extras["per_config"] = per_cfg
@@ -437,7 +449,7 @@ def run_single(args):
     peaks, _ = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     name = args.workload
-    if name in workloads.S6:
+    if name in workloads.S6 or (name.endswith("_state") and name[:-6] in workloads.S6):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         sfu = mufu_probe(torch, ss, dev, sms) if not args.no_extras else 9.86e12
         r = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream, hbm_peak, sfu)
@@ -470,7 +482,7 @@ def main():
                     help="with --workload affine_*: use this many elements (small ncu captures)")
     ap.add_argument("--workload", default=HEADLINE,
                     help="time one workload only (affine_small, affine_large, s6_fp32, "
-                         "s6_bf16, s6_bidir); the default is the full benchmark")
+                         "s6_bf16, s6_bidir, s6_bf16_state); the default is the full benchmark")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -169,6 +169,33 @@ ss_status ss_selective_scan_bidir(const void *x, const void *delta,
                                   void *workspace, size_t workspace_bytes,
                                   void *stream);
 
+/*
+ * Forward scan that starts from a given state and returns the final one, so
+ * a long sequence can be run in pieces (streaming inference, or a sequence
+ * longer than one call should hold): running [0, L1) and then [L1, L) with
+ * the first call's h_last as the second call's h0 computes the same
+ * recurrence as running [0, L) in one call (equal up to fp32 rounding; the
+ * two orders of fma differ). The pages fix the state before t = 0 at zero
+ * ("POPCORNBENCH FW-GLM-5-1 l2_p30", forward-pass derivation); this entry
+ * point generalises that one step, which they leave open.
+ * Arguments as ss_selective_scan_fwd, plus:
+ *   h0:     (B, D, N) fp32 device array, row-major, the state h[-1] of every
+ *           (b, d, n) chain; NULL means zeros.
+ *   h_last: (B, D, N) fp32 device array receiving h[L-1]; NULL means not
+ *           written. Must not alias h0 or any other argument.
+ * Both are caller-owned and 4-byte aligned (else SS_ERR_INVALID). The
+ * workspace is the one ss_selective_scan_workspace_bytes(..., bidir = 0)
+ * asks for. With L == 0 the call copies nothing: h_last is left unwritten.
+ */
+ss_status ss_selective_scan_fwd_state(const void *x, const void *delta,
+                                      const void *Bt, const void *Ct,
+                                      const float *A, const float *Dskip,
+                                      const float *h0, void *y, float *h_last,
+                                      int64_t B, int64_t L, int64_t D, int64_t N,
+                                      int io_dtype, int delta_softplus,
+                                      void *workspace, size_t workspace_bytes,
+                                      void *stream);
+
 /* ------------------------------------------------------------ errors */
 
 /*

@@ -27,7 +27,7 @@ __all__ = [
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
-    "new_workspace", "EXPORTED_SYMBOLS",
+    "ss_selective_scan_fwd_state", "new_workspace", "EXPORTED_SYMBOLS",
 ]
 
 SS_OK, SS_ERR_INVALID, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -38,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
-    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc",
+    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_selective_scan_fwd_state",
 )
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -98,6 +98,9 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_probe_mufu_ex2.restype = ci
     L.ss_affine_scan_noalloc.argtypes = [vp, vp, vp, i64, vp]
     L.ss_affine_scan_noalloc.restype = ci
+    L.ss_selective_scan_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
+                                              i64, ci, ci, vp, sz, vp]
+    L.ss_selective_scan_fwd_state.restype = ci
     return L
 
 
@@ -236,7 +239,8 @@ def ss_selective_scan_workspace_bytes(B, L, D, N, io_dtype=SS_F32, bidir=False) 
                                                    int(io_dtype), int(bool(bidir)))
 
 
-def _s6(fn_name, x, delta, Bt, Ct, A, Dskip, delta_softplus, y, workspace, stream, bidir):
+def _s6(fn_name, x, delta, Bt, Ct, A, Dskip, delta_softplus, y, workspace, stream, bidir,
+        state=None):
     torch = _torch()
     io = (torch.float32, torch.bfloat16)
     for t, nm in ((x, "x"), (delta, "delta"), (Bt, "Bt"), (Ct, "Ct")):
@@ -266,9 +270,20 @@ def _s6(fn_name, x, delta, Bt, Ct, A, Dskip, delta_softplus, y, workspace, strea
         key = (fn_name, B, L, D, N, io_dtype, need, os.environ.get("SS_S6_WT_TSUB"))
         workspace = _cached_workspace(key, need, x.device, sh)
     wsb = workspace.numel() if workspace is not None else 0
-    st = getattr(lib(), fn_name)(_ptr(x), _ptr(delta), _ptr(Bt), _ptr(Ct), _ptr(A), _ptr(Dskip),
-                                 _ptr(y), B, L, D, N, io_dtype, int(bool(delta_softplus)),
-                                 _ptr(workspace), wsb, sh)
+    if state is not None:  # (h0, h_last) of the forward-with-state call
+        h0, h_last = state
+        for t, nm in ((h0, "h0"), (h_last, "h_last")):
+            if t is not None:
+                _check_cuda(t, nm, (torch.float32,))
+                if tuple(t.shape) != (B, D, N):
+                    raise ValueError(f"{nm} must be (B, D, N) = {(B, D, N)}")
+        st = lib().ss_selective_scan_fwd_state(
+            _ptr(x), _ptr(delta), _ptr(Bt), _ptr(Ct), _ptr(A), _ptr(Dskip), _ptr(h0), _ptr(y),
+            _ptr(h_last), B, L, D, N, io_dtype, int(bool(delta_softplus)), _ptr(workspace), wsb, sh)
+    else:
+        st = getattr(lib(), fn_name)(_ptr(x), _ptr(delta), _ptr(Bt), _ptr(Ct), _ptr(A),
+                                     _ptr(Dskip), _ptr(y), B, L, D, N, io_dtype,
+                                     int(bool(delta_softplus)), _ptr(workspace), wsb, sh)
     if st != SS_OK:
         raise SSError(st, fn_name)
     return y
@@ -279,6 +294,19 @@ def ss_selective_scan_fwd(x, delta, Bt, Ct, A, Dskip=None, delta_softplus=False,
     """S6 selective-scan forward; returns y (B, L, D) in x's dtype."""
     return _s6("ss_selective_scan_fwd", x, delta, Bt, Ct, A, Dskip, delta_softplus, y,
                workspace, stream, False)
+
+
+def ss_selective_scan_fwd_state(x, delta, Bt, Ct, A, Dskip=None, h0=None, delta_softplus=False,
+                                y=None, h_last=None, workspace=None, stream=None):
+    """S6 forward from the state h0 ((B, D, N) fp32, zeros if None); returns
+    (y, h_last) with h_last (B, D, N) fp32 the state after the last step."""
+    torch = _torch()
+    if h_last is None:
+        B, _, D = x.shape
+        h_last = torch.empty((B, D, A.shape[1]), dtype=torch.float32, device=x.device)
+    y = _s6("ss_selective_scan_fwd", x, delta, Bt, Ct, A, Dskip, delta_softplus, y,
+            workspace, stream, False, state=(h0, h_last))
+    return y, h_last
 
 
 def ss_selective_scan_bidir(x, delta, Bt, Ct, A, Dskip=None, delta_softplus=False, y=None,

@@ -80,6 +80,8 @@ struct S6Params {
     float *payload;    // [((seq*K + k)*NF + field)*32*NG + lane*NG + i]
     unsigned long long timeout_ns;
     long long skip_unit;  // test hook: this unit publishes nothing (-1: none)
+    const float *h0;      // (B, D, N) state before t = 0, or null (zeros); forward only
+    float *h_last;        // (B, D, N) receives the state after t = L - 1, or null
 };
 
 // ------------------------------------------------------------------ f32x2
@@ -313,7 +315,9 @@ __device__ __forceinline__ void step(float xv, float dv, const float *brow, cons
         }
         const u64 acc = f2add(acc0, acc1);
         float accs = f2lo(acc) + f2hi(acc);
-        if constexpr (LPC == 2) accs += __shfl_xor_sync(0xffffffffu, accs, 1);  // other state half
+#pragma unroll
+        for (int o = 1; o < LPC; o <<= 1)  // the channel's other state slices
+            accs += __shfl_xor_sync(0xffffffffu, accs, o);
         const float yv = fmaf(Dd, xv, accs);
         if (store) {
             if constexpr (OUT == OUT_Y) store_io(yp, yv);
@@ -562,6 +566,11 @@ __device__ __forceinline__ float4 apply_quads(const S6Params &p, int NF, long lo
     return c;
 }
 
+// State n of this lane's channel before t = 0: h0 if given, else zero.
+__device__ __forceinline__ float initial_state(const S6Params &p, const WarpCtx &w, int n) {
+    return (p.h0 && w.dvalid && n < p.N) ? p.h0[(w.b * p.D + w.d) * p.N + n] : 0.0f;
+}
+
 // ------------------------------------------------------------------ kernel
 template <int NG, int LPC, typename IO, bool SP, bool BIDIR>
 __global__ void __launch_bounds__(kMaxWT * 32, 3)
@@ -625,9 +634,13 @@ s6_kernel(const __grid_constant__ S6Params p) {
 
     u64 h[NP], hr[NP], Q[NP];
     float sdel = 0.0f;
+    // state entering the sequence: h0, or zero
     float cf[NG], cr[NG];
 #pragma unroll
-    for (int i = 0; i < NG; ++i) cf[i] = cr[i] = 0.0f;
+    for (int i = 0; i < NG; ++i) {
+        cf[i] = BIDIR ? 0.0f : initial_state(p, w, w.half * NG + i);
+        cr[i] = 0.0f;
+    }
 
     if (chunked || p.WT > 1) {
         // ---- sub-chunk aggregate from a zero state
@@ -681,6 +694,11 @@ s6_kernel(const __grid_constant__ S6Params p) {
             for (int qd = warp; qd < NG / 4; qd += p.WT) {
                 float4 c = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 if (j >= 0) c = ld_cg_f32x4(quad_ptr(field_ptr<NG>(p, NF, seq * p.K + j, F_INC, lane), qd));
+                if (j == -1 && !BIDIR) {  // the sequence's start: h0
+                    const int n0 = w.half * NG + 4 * qd;
+                    c = make_float4(initial_state(p, w, n0), initial_state(p, w, n0 + 1),
+                                    initial_state(p, w, n0 + 2), initial_state(p, w, n0 + 3));
+                }
                 if (j != -2) c = apply_quads<NG>(p, NF, seq, j + 1, k, 1, F_H, lane, qd, c);
                 s_car[(4 * qd) * 32 + lane] = c.x;
                 s_car[(4 * qd + 1) * 32 + lane] = c.y;
@@ -762,6 +780,16 @@ s6_kernel(const __grid_constant__ S6Params p) {
             sweep<NG, LPC, IO, SP, BIDIR, MODE_OUT, false, OUT_Y, true>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
         else
             sweep<NG, LPC, IO, SP, BIDIR, MODE_OUT, false, OUT_Y>(p, w, A2, Dd, h, hr, Q, sdel, nullptr);
+        // the warp that ran the last step holds h[L - 1]
+        if (p.h_last && w.dvalid && w.t0 < w.t1 && w.t1 == p.L) {
+            float *dst = p.h_last + (w.b * p.D + w.d) * p.N;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const int n0 = w.half * NG + 2 * q;
+                if (n0 < p.N) dst[n0] = f2lo(h[q]);
+                if (n0 + 1 < p.N) dst[n0 + 1] = f2hi(h[q]);
+            }
+        }
     }
 
     if (chunked) finish_launch(p.ws, tag);
@@ -793,10 +821,11 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     // Two lanes per channel (8 states each) doubles the warps but repeats the
     // per-timestep scalar work on both lanes; measured slower on every S6
     // shape tried, so it is only taken on request.
-    if (const char *e = std::getenv("SS_S6_LPC")) {  // tuning override: 1 or 2
-        if (std::atoi(e) == 2 && pl.NG == 16) {
-            pl.NG = 8;
-            pl.LPC = 2;
+    if (const char *e = std::getenv("SS_S6_LPC")) {  // tuning override: 1, 2 or 4
+        const int v = std::atoi(e);
+        if ((v == 2 || v == 4) && pl.NG == 16) {
+            pl.NG = 16 / v;
+            pl.LPC = v;
         }
     }
     const int cpw = 32 / pl.LPC;
@@ -912,6 +941,7 @@ ss_status launch_ng(const S6Params &prm, const Plan &pl, bool sp, bool bidir, cu
 template <typename IO>
 ss_status launch_io(const S6Params &prm, const Plan &pl, bool sp, bool bidir, cudaStream_t s) {
     if (pl.LPC == 2) return launch_ng<8, 2, IO>(prm, pl, sp, bidir, s);
+    if (pl.LPC == 4) return launch_ng<4, 4, IO>(prm, pl, sp, bidir, s);
     switch (pl.NG) {
         case 4: return launch_ng<4, 1, IO>(prm, pl, sp, bidir, s);
         case 8: return launch_ng<8, 1, IO>(prm, pl, sp, bidir, s);
@@ -966,6 +996,8 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
     }
     prm.timeout_ns = timeout_ns;
     prm.skip_unit = skip_unit;
+    prm.h0 = a.bidir ? nullptr : a.h0;
+    prm.h_last = a.bidir ? nullptr : a.h_last;
     char *ws = static_cast<char *>(workspace);
     prm.ws = reinterpret_cast<WsHeader *>(ws);
     prm.flags = pl.K > 1 ? reinterpret_cast<unsigned *>(ws + kWsHeaderBytes) : nullptr;

@@ -20,7 +20,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 ss_status s6_entry(const void *x, const void *delta, const void *Bt, const void *Ct, const float *A,
                    const float *Dskip, void *y, int64_t B, int64_t L, int64_t D, int64_t N,
                    int io_dtype, int delta_softplus, void *workspace, size_t workspace_bytes,
-                   void *stream, int bidir) {
+                   void *stream, int bidir, const float *h0 = nullptr, float *h_last = nullptr) {
     if (B < 0 || L < 0 || D < 0 || N < 0) return SS_ERR_INVALID;
     if (io_dtype != SS_F32 && io_dtype != SS_BF16) return SS_ERR_INVALID;
     if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
@@ -28,7 +28,8 @@ ss_status s6_entry(const void *x, const void *delta, const void *Bt, const void 
     if (!x || !delta || !Bt || !Ct || !A || !y) return SS_ERR_INVALID;
     const uintptr_t es = io_dtype == SS_BF16 ? 2 : 4;
     if (!aligned(x, es) || !aligned(delta, es) || !aligned(Bt, es) || !aligned(Ct, es) ||
-        !aligned(y, es) || !aligned(A, 4) || (Dskip && !aligned(Dskip, 4)))
+        !aligned(y, es) || !aligned(A, 4) || (Dskip && !aligned(Dskip, 4)) ||
+        (h0 && !aligned(h0, 4)) || (h_last && !aligned(h_last, 4)))
         return SS_ERR_INVALID;
     if (B > (1LL << 31) || L > (1LL << 40) || D > (1LL << 31) || B * L > (1LL << 48))
         return SS_ERR_UNSUPPORTED;
@@ -40,6 +41,8 @@ ss_status s6_entry(const void *x, const void *delta, const void *Bt, const void 
     a.A = A;
     a.Dskip = Dskip;
     a.y = y;
+    a.h0 = h0;
+    a.h_last = h_last;
     a.B = B;
     a.L = L;
     a.D = D;
@@ -108,6 +111,16 @@ ss_status ss_selective_scan_bidir(const void *x, const void *delta, const void *
                                   void *workspace, size_t workspace_bytes, void *stream) {
     return s6_entry(x, delta, Bt, Ct, A, Dskip, y, B, L, D, N, io_dtype, delta_softplus, workspace,
                     workspace_bytes, stream, 1);
+}
+
+ss_status ss_selective_scan_fwd_state(const void *x, const void *delta, const void *Bt,
+                                      const void *Ct, const float *A, const float *Dskip,
+                                      const float *h0, void *y, float *h_last, int64_t B,
+                                      int64_t L, int64_t D, int64_t N, int io_dtype,
+                                      int delta_softplus, void *workspace, size_t workspace_bytes,
+                                      void *stream) {
+    return s6_entry(x, delta, Bt, Ct, A, Dskip, y, B, L, D, N, io_dtype, delta_softplus, workspace,
+                    workspace_bytes, stream, 0, h0, h_last);
 }
 
 ss_status ss_get_device_status(void *workspace, void *stream) {

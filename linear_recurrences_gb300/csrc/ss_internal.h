@@ -17,6 +17,8 @@ struct S6Args {
     const void *x, *delta, *Bt, *Ct;
     const float *A, *Dskip;
     void *y;
+    const float *h0;  // (B, D, N) initial state or null (zeros); forward only
+    float *h_last;    // (B, D, N) final state or null; forward only
     int64_t B, L, D, N;
     int io_bf16;
     int softplus;

@@ -82,6 +82,19 @@ def test_s6_argument_errors(L):
     assert L.ss_selective_scan_workspace_bytes(2, 8, 4, 17, 0, 0) == 0
 
 
+def test_s6_state_argument_errors(L):
+    p = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(258)  # not 4-byte aligned
+    fn = L.ss_selective_scan_fwd_state
+    args = lambda h0, hl, B=2, L_=8, D=4, N=16: (
+        p, p, p, p, p, None, h0, p, hl, B, L_, D, N, 0, 0, None, 0, None)
+    assert fn(*args(odd, p)) == ss.SS_ERR_INVALID
+    assert fn(*args(p, odd)) == ss.SS_ERR_INVALID
+    assert fn(*args(None, None, N=17)) == ss.SS_ERR_UNSUPPORTED
+    assert fn(*args(p, p, L_=0)) == ss.SS_OK  # empty: nothing launched, nothing written
+    assert fn(*args(p, p, B=-1)) == ss.SS_ERR_INVALID
+
+
 def test_spin_timeout(L):
     assert L.ss_set_spin_timeout_ns(0) == ss.SS_ERR_INVALID
     assert L.ss_set_spin_timeout_ns(10**9) == ss.SS_OK

@@ -220,7 +220,7 @@ def test_timeout_is_reported_not_hung(torch, ss, plan_override, bidir):
 
 @pytest.fixture
 def lane_layout():
-    """Forces one or two lanes per channel (SS_S6_LPC) for one test."""
+    """Forces one, two or four lanes per channel (SS_S6_LPC) for one test."""
     old = os.environ.get("SS_S6_LPC")
 
     def set_(v):
@@ -232,12 +232,12 @@ def lane_layout():
         os.environ["SS_S6_LPC"] = old
 
 
-@pytest.mark.parametrize("lpc", [1, 2])
+@pytest.mark.parametrize("lpc", [1, 2, 4])
 @pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
 @pytest.mark.parametrize("io,softplus", [("f32", False), ("bf16", True)])
 def test_both_lane_layouts(torch, ss, lane_layout, plan_override, lpc, bidir, io, softplus):
-    """16 states per lane, or 8 states on each of two lanes per channel; the
-    register path (one warp over all of L) and a chunked plan."""
+    """16 states per lane, or 8 / 4 states on each of two / four lanes per
+    channel; the register path (one warp over all of L) and a chunked plan."""
     lane_layout(lpc)
     for wt_tsub in (None, (2, 24)):
         if wt_tsub:
