@@ -69,6 +69,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_s6_fwd_state_f64.argtypes = [f, f, f, f, f, f, dp, dp, dp, i64, i64, i64, i64,
                                             ctypes.c_int, ctypes.c_int]
     lib.oracle_s6_fwd_state_f64.restype = ctypes.c_int
+    lib.oracle_s6_bwd_f64.argtypes = [f, f, f, f, f, f, dp, f, dp, i64, i64, i64, i64,
+                                      ctypes.c_int, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int]
+    lib.oracle_s6_bwd_f64.restype = ctypes.c_int
     lib.oracle_s6_channels_f64.argtypes = [
         f, f, f, f, f, f, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
         ctypes.POINTER(ctypes.c_int64), i64, dp, ctypes.c_int]
@@ -181,4 +184,36 @@ def s6_channels(x, delta, Bt, Ct, A, Dskip, chans, softplus=False, bidir=False,
         ch.shape[0], _p(out, ctypes.c_double), int(threads))
     if rc:
         raise RuntimeError(f"oracle_s6_channels_f64 failed ({rc})")
+    return out
+
+
+def s6_bwd(x, delta, Bt, Ct, A, Dskip, dy, h0=None, dh_last=None, softplus=False, threads=1,
+           lib: ctypes.CDLL | None = None) -> dict:
+    """Gradients of sum(dy * y) + sum(dh_last * h_last) for the S6 forward
+    from h0, in float64: dict with dx, ddelta (B, L, D), dA (D, N),
+    dBt, dCt (B, L, N), dDskip (D,), dh0 (B, D, N)."""
+    lib = lib or load()
+    x, delta, Bt, Ct, A, Dskip, B, L, D, N = _s6_args(x, delta, Bt, Ct, A, Dskip)
+    dy = _f32(dy)
+    if dy.shape != (B, L, D):
+        raise ValueError("dy must be (B, L, D)")
+
+    def state(v, name):
+        if v is None:
+            return None
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        if v.shape != (B, D, N):
+            raise ValueError(f"{name} must be (B, D, N)")
+        return v
+    h0, dh_last = state(h0, "h0"), state(dh_last, "dh_last")
+    out = {"dx": np.zeros((B, L, D)), "ddelta": np.zeros((B, L, D)), "dA": np.zeros((D, N)),
+           "dBt": np.zeros((B, L, N)), "dCt": np.zeros((B, L, N)), "dDskip": np.zeros(D),
+           "dh0": np.zeros((B, D, N))}
+    dp = lambda v: None if v is None else _p(v, ctypes.c_double)
+    rc = lib.oracle_s6_bwd_f64(_p(x), _p(delta), _p(Bt), _p(Ct), _p(A), _p(Dskip), dp(h0), _p(dy),
+                               dp(dh_last), B, L, D, N, int(bool(softplus)),
+                               *(dp(out[k]) for k in ("dx", "ddelta", "dA", "dBt", "dCt",
+                                                      "dDskip", "dh0")), int(threads))
+    if rc:
+        raise RuntimeError(f"oracle_s6_bwd_f64 failed ({rc})")
     return out

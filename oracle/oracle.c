@@ -247,3 +247,163 @@ int oracle_s6_channels_f64(const float *x, const float *delta, const float *Bt,
                 chans, nchan, NULL, NULL, out, 0, 0};
     return s6_run(j, threads);
 }
+
+
+/* ------------------------------------------------------------------ backward */
+
+/* Reverse-mode derivative of the forward pass from h0 (the scope table's
+ * "next" row; the pages give only the forward pass, so this is the exact
+ * derivative of that definition, taken step by step in reverse order) for the
+ * scalar loss  sum_{b,t,d} dy*y + sum_{b,d,n} dh_last*h_last.
+ * Forward per (b, d), as above:  dl = sp(v) or v;  dA = exp(dl*A[d,n]);
+ *   h_t = dA*h_{t-1} + dl*B_t*x;  y_t = sum_n h_t*C_t + D*x.
+ * Reverse, with g[n] the gradient reaching h_t from later steps (starting
+ * from dh_last) and lam = g + dy_t*C_t the whole gradient of h_t:
+ *   dC_t += dy_t*h_t;  dD += dy_t*x;  dx_t = dy_t*D + sum_n lam*dl*B_t;
+ *   ddl_t = sum_n lam*(B_t*x + h_{t-1}*dA*A);  dA_param += lam*h_{t-1}*dA*dl;
+ *   dB_t += lam*dl*x;  g = lam*dA (the gradient of h_{t-1});  dh0 = final g.
+ *   dv = ddl * sigmoid(v) under softplus (v > 20: ddl).
+ * dx, ddelta: (B, L, D); dA: (D, N); dBt, dCt: (B, L, N); dDskip: (D,);
+ * dh0: (B, D, N) or NULL; h0, dh_last: (B, D, N) or NULL (zeros). */
+typedef struct {
+    const float *x, *delta, *Bt, *Ct, *A, *Dskip, *dy;
+    const double *h0, *dh_last;
+    int64_t B, L, D, N;
+    int softplus;
+    double *dx, *ddelta, *dA, *dBt, *dCt, *dDskip, *dh0;
+    int64_t b0, b1;          /* batch range of this worker */
+    double *dA_part, *dD_part; /* this worker's sums over its batch range */
+} s6_bwd_job;
+
+static void *s6_bwd_worker(void *arg)
+{
+    s6_bwd_job *j = (s6_bwd_job *)arg;
+    const int64_t L = j->L, D = j->D, N = j->N;
+    double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N));  /* h_{-1} .. h_{L-1} */
+    double *dAs = (double *)malloc(sizeof(double) * (size_t)(L * N));
+    double *dls = (double *)malloc(sizeof(double) * (size_t)L);
+    double *g = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!hs || !dAs || !dls || !g) {
+        free(hs); free(dAs); free(dls); free(g);
+        return (void *)1;
+    }
+    for (int64_t b = j->b0; b < j->b1; ++b) {
+        for (int64_t d = 0; d < D; ++d) {
+            const double Dd = (double)j->Dskip[d];
+            /* forward, keeping every state and every dA */
+            for (int64_t n = 0; n < N; ++n)
+                hs[n] = j->h0 ? j->h0[(b * D + d) * N + n] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                const int64_t xi = (b * L + t) * D + d, bi = (b * L + t) * N;
+                double dl = (double)j->delta[xi];
+                if (j->softplus)
+                    dl = oracle_softplus_f64(dl);
+                dls[t] = dl;
+                const double xv = (double)j->x[xi];
+                for (int64_t n = 0; n < N; ++n) {
+                    const double dA = exp(dl * (double)j->A[d * N + n]);
+                    dAs[t * N + n] = dA;
+                    hs[(t + 1) * N + n] = dA * hs[t * N + n] + dl * (double)j->Bt[bi + n] * xv;
+                }
+            }
+            /* reverse */
+            for (int64_t n = 0; n < N; ++n)
+                g[n] = j->dh_last ? j->dh_last[(b * D + d) * N + n] : 0.0;
+            for (int64_t t = L - 1; t >= 0; --t) {
+                const int64_t xi = (b * L + t) * D + d, bi = (b * L + t) * N;
+                const double gy = (double)j->dy[xi], xv = (double)j->x[xi], dl = dls[t];
+                double gx = gy * Dd, gdl = 0.0;
+                j->dD_part[d] += gy * xv;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double Bv = (double)j->Bt[bi + n], Cv = (double)j->Ct[bi + n];
+                    const double ht = hs[(t + 1) * N + n], hprev = hs[t * N + n];
+                    const double dA = dAs[t * N + n], An = (double)j->A[d * N + n];
+                    const double lam = g[n] + gy * Cv;
+                    j->dCt[bi + n] += gy * ht;
+                    gx += lam * dl * Bv;
+                    gdl += lam * (Bv * xv + hprev * dA * An);
+                    j->dA_part[d * N + n] += lam * hprev * dA * dl;
+                    j->dBt[bi + n] += lam * dl * xv;
+                    g[n] = lam * dA;
+                }
+                j->dx[xi] = gx;
+                if (j->softplus) {
+                    const double v = (double)j->delta[xi];
+                    gdl = v > 20.0 ? gdl : gdl / (1.0 + exp(-v));
+                }
+                j->ddelta[xi] = gdl;
+            }
+            if (j->dh0)
+                for (int64_t n = 0; n < N; ++n)
+                    j->dh0[(b * D + d) * N + n] = g[n];
+        }
+    }
+    free(hs); free(dAs); free(dls); free(g);
+    return NULL;
+}
+
+/* Splits the batch over `threads` workers; each keeps its own dA and dDskip
+ * sums, added in worker order at the end. Returns 0 on success. */
+int oracle_s6_bwd_f64(const float *x, const float *delta, const float *Bt,
+                      const float *Ct, const float *A, const float *Dskip,
+                      const double *h0, const float *dy, const double *dh_last,
+                      int64_t B, int64_t L, int64_t D, int64_t N, int softplus,
+                      double *dx, double *ddelta, double *dA, double *dBt,
+                      double *dCt, double *dDskip, double *dh0, int threads)
+{
+    if (B <= 0 || L < 0 || D <= 0 || N <= 0)
+        return 0;
+    if (threads < 1)
+        threads = 1;
+    if (threads > B)
+        threads = (int)B;
+    for (int64_t i = 0; i < B * L * N; ++i)
+        dBt[i] = dCt[i] = 0.0;
+    s6_bwd_job *jobs = (s6_bwd_job *)calloc((size_t)threads, sizeof(s6_bwd_job));
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)threads);
+    double *parts = (double *)calloc((size_t)threads * (size_t)(D * N + D), sizeof(double));
+    if (!jobs || !tid || !parts) {
+        free(jobs); free(tid); free(parts);
+        return -1;
+    }
+    int rc = 0, started = 0;
+    for (int i = 0; i < threads; ++i) {
+        s6_bwd_job jb = {x, delta, Bt, Ct, A, Dskip, dy, h0, dh_last, B, L, D, N, softplus,
+                         dx, ddelta, dA, dBt, dCt, dDskip, dh0,
+                         B * i / threads, B * (i + 1) / threads,
+                         parts + (size_t)i * (size_t)(D * N + D),
+                         parts + (size_t)i * (size_t)(D * N + D) + D * N};
+        jobs[i] = jb;
+        if (threads == 1) {
+            if (s6_bwd_worker(&jobs[0]))
+                rc = -1;
+            started = 0;
+            break;
+        }
+        if (pthread_create(&tid[i], NULL, s6_bwd_worker, &jobs[i]) != 0) {
+            rc = -1;
+            break;
+        }
+        ++started;
+    }
+    for (int i = 0; i < started; ++i) {
+        void *ret = NULL;
+        pthread_join(tid[i], &ret);
+        if (ret)
+            rc = -1;
+    }
+    for (int64_t k = 0; k < D * N; ++k) {
+        double s = 0.0;
+        for (int i = 0; i < threads; ++i)
+            s += parts[(size_t)i * (size_t)(D * N + D) + k];
+        dA[k] = s;
+    }
+    for (int64_t k = 0; k < D; ++k) {
+        double s = 0.0;
+        for (int i = 0; i < threads; ++i)
+            s += parts[(size_t)i * (size_t)(D * N + D) + D * N + k];
+        dDskip[k] = s;
+    }
+    free(jobs); free(tid); free(parts);
+    return rc;
+}

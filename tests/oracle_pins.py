@@ -386,6 +386,94 @@ S6_PINS = [pin_s6_matrix_form, pin_s6_bidir_matrix_form, pin_s6_A_zero,
 ALL_PINS = AFFINE_PINS + S6_PINS
 
 
+# ---------------------------------------------------------------- backward pins
+def _dyadic_s6(seed, B=2, L=5, D=3, N=4, softplus=False):
+    """Inputs that are multiples of 2**-6 (delta: 2**-8) in small ranges, so
+    that moving any of them by 2**-14 is exact in float32."""
+    g = _rng(seed)
+    dy = lambda *sh: _dyadic(g, int(np.prod(sh)), -2.0, 2.0, 6).reshape(sh)
+    x, Bt, Ct, dyv = dy(B, L, D), dy(B, L, N), dy(B, L, N), dy(B, L, D)
+    if softplus:
+        dl = _dyadic(g, B * L * D, -3.0, 2.0, 6).reshape(B, L, D)
+    else:
+        dl = _dyadic(g, B * L * D, 2.0 ** -6, 1.0, 8).reshape(B, L, D)
+    A = _dyadic(g, D * N, -3.0, -0.25, 6).reshape(D, N)
+    Ds = _dyadic(g, D, -1.0, 1.0, 6)
+    h0 = g.integers(-64, 65, (B, D, N)) / 32.0
+    dhl = g.integers(-64, 65, (B, D, N)) / 32.0
+    return [x, dl, Bt, Ct, A, Ds], h0, dyv, dhl
+
+
+def _loss(lib, args, h0, dyv, dhl, softplus):
+    y, hl = oracle.s6_fwd_state(*args, h0=h0, softplus=softplus, lib=lib)
+    return math.fsum((y * dyv.astype(np.float64)).ravel()) + math.fsum((hl * dhl).ravel())
+
+
+def _check_fd(lib, seed, softplus):
+    args, h0, dyv, dhl = _dyadic_s6(seed, softplus=softplus)
+    gr = oracle.s6_bwd(*args, dyv, h0=h0, dh_last=dhl, softplus=softplus, lib=lib)
+    eps = 2.0 ** -14
+    names = ["dx", "ddelta", "dBt", "dCt", "dA", "dDskip"]
+    for k, name in enumerate(names):
+        src = {0: 0, 1: 1, 2: 2, 3: 3, 4: 4, 5: 5}[k]
+        for idx in np.ndindex(args[src].shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[src][idx] += np.float32(eps)
+            minus[src][idx] -= np.float32(eps)
+            assert plus[src][idx] - minus[src][idx] == np.float32(2 * eps), "exact perturbation"
+            fd = (_loss(lib, plus, h0, dyv, dhl, softplus)
+                  - _loss(lib, minus, h0, dyv, dhl, softplus)) / (2 * eps)
+            an = gr[name][idx]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), f"{name}{idx}: fd {fd} vs {an}"
+    for idx in np.ndindex(h0.shape):
+        hp, hm = h0.copy(), h0.copy()
+        hp[idx] += eps
+        hm[idx] -= eps
+        fd = (_loss(lib, args, hp, dyv, dhl, softplus)
+              - _loss(lib, args, hm, dyv, dhl, softplus)) / (2 * eps)
+        an = gr["dh0"][idx]
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), f"dh0{idx}: fd {fd} vs {an}"
+
+
+def pin_bwd_finite_differences(lib):
+    _check_fd(lib, 30, softplus=False)
+
+
+def pin_bwd_finite_differences_softplus(lib):
+    _check_fd(lib, 31, softplus=True)
+
+
+def pin_bwd_euler_and_skip(lib):
+    """y and h_last are linear in x (h0 = 0), in Bt, in Ct and in h0 (x = 0),
+    so sum(v * dL/dv) recovers the matching part of the loss exactly; and
+    dDskip[d] = sum over (b, t) of dy * x."""
+    args, h0, dyv, dhl = _dyadic_s6(32, L=7)
+    x, dl, Bt, Ct, A, Ds = args
+    f64 = lambda v: v.astype(np.float64)
+    y, hl = oracle.s6_fwd_state(*args, lib=lib)
+    gr = oracle.s6_bwd(*args, dyv, dh_last=dhl, lib=lib)
+    loss = math.fsum((y * f64(dyv)).ravel()) + math.fsum((hl * dhl).ravel())
+    skip = math.fsum((f64(x) * f64(Ds) * f64(dyv)).ravel())
+    chk = lambda a, b, what: abs(a - b) <= 1e-12 * max(1.0, abs(b))
+    assert chk(math.fsum((f64(x) * gr["dx"]).ravel()), loss, "x"), "Euler identity in x"
+    assert chk(math.fsum((f64(Bt) * gr["dBt"]).ravel()), loss - skip, "B"), "Euler identity in Bt"
+    assert chk(math.fsum((f64(Ct) * gr["dCt"]).ravel()),
+               math.fsum((y * f64(dyv)).ravel()) - skip, "C"), "Euler identity in Ct"
+    assert np.allclose(gr["dDskip"], (f64(dyv) * f64(x)).sum(axis=(0, 1)), rtol=0, atol=1e-13), \
+        "dDskip closed form"
+    z = np.zeros_like(x)
+    y0, hl0 = oracle.s6_fwd_state(z, dl, Bt, Ct, A, Ds, h0=h0, lib=lib)
+    g0 = oracle.s6_bwd(z, dl, Bt, Ct, A, Ds, dyv, h0=h0, dh_last=dhl, lib=lib)
+    loss0 = math.fsum((y0 * f64(dyv)).ravel()) + math.fsum((hl0 * dhl).ravel())
+    assert chk(math.fsum((h0 * g0["dh0"]).ravel()), loss0, "h0"), "Euler identity in h0"
+
+
+BWD_PINS = [pin_bwd_finite_differences, pin_bwd_finite_differences_softplus,
+            pin_bwd_euler_and_skip]
+ALL_PINS = ALL_PINS + BWD_PINS
+
+
 def failures(lib) -> list[str]:
     """Names of the pins that fail (or crash) for this oracle library."""
     bad = []

@@ -53,6 +53,19 @@ MUTANTS = [
     ("state_hlast_is_h0",
      "j->hlast[(b * D + d) * N + n] = h[n];",
      "j->hlast[(b * D + d) * N + n] = j->h0 ? j->h0[(b * D + d) * N + n] : 0.0;", 1),
+    ("bwd_hprev_is_h_t",
+     "const double ht = hs[(t + 1) * N + n], hprev = hs[t * N + n];",
+     "const double ht = hs[(t + 1) * N + n], hprev = hs[(t + 1) * N + n];", 1),
+    ("bwd_ddelta_drops_A",
+     "gdl += lam * (Bv * xv + hprev * dA * An);", "gdl += lam * (Bv * xv + hprev * dA);", 1),
+    ("bwd_sigmoid_sign",
+     "gdl / (1.0 + exp(-v))", "gdl / (1.0 + exp(v))", 1),
+    ("bwd_dB_drops_delta",
+     "j->dBt[bi + n] += lam * dl * xv;", "j->dBt[bi + n] += lam * xv;", 1),
+    ("bwd_adjoint_not_decayed",
+     "g[n] = lam * dA;", "g[n] = lam;", 1),
+    ("bwd_dC_uses_adjoint",
+     "j->dCt[bi + n] += gy * ht;", "j->dCt[bi + n] += lam * ht;", 1),
     ("bidir_reverse_state_not_reset",
      "    /* reverse: t = L-1 .. 0, h_rev[t] = dA[t]*h_rev[t+1] + dBx[t] */\n"
      "    for (int64_t n = 0; n < N; ++n)\n        h[n] = 0.0;\n",
