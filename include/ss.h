@@ -196,6 +196,42 @@ ss_status ss_selective_scan_fwd_state(const void *x, const void *delta,
                                       void *workspace, size_t workspace_bytes,
                                       void *stream);
 
+/*
+ * Backward pass of ss_selective_scan_fwd_state: the gradients of the scalar
+ * sum_{b,t,d} dy*y + sum_{b,d,n} dh_last*h_last with respect to every input,
+ * i.e. the exact derivative of the forward recurrence ("POPCORNBENCH
+ * FW-GLM-5-1 l2_p30", forward-pass derivation; the pages give no backward
+ * pass, so this is that definition differentiated). The adjoint of h runs in
+ * reverse time over the same dA: lam_t = dy_t*C_t + dA_{t+1}*lam_{t+1}.
+ * Inputs as ss_selective_scan_fwd_state (h0 may be NULL), plus
+ *   dy:      (B, L, D) of io_dtype, the gradient of y;
+ *   dh_last: (B, D, N) fp32 gradient of h_last, or NULL (zeros).
+ * Outputs, all caller-owned device arrays, fully overwritten:
+ *   dx, ddelta: (B, L, D) of io_dtype (ddelta is the gradient of the delta
+ *               input, through softplus when delta_softplus != 0);
+ *   dA: (D, N) fp32;  dBt, dCt: (B, L, N) fp32;
+ *   dDskip: (D,) fp32, or NULL to skip it;  dh0: (B, D, N) fp32, or NULL.
+ * Every sum over channels or time is taken in a fixed order: results are
+ * bitwise reproducible. Outputs must not alias inputs or each other. The
+ * workspace (ss_selective_scan_bwd_workspace_bytes) needs no zeroing.
+ * Four launches on `stream`: chunk aggregates, carries across chunks,
+ * gradients, and the final fixed-order sums.
+ */
+size_t ss_selective_scan_bwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N);
+
+ss_status ss_selective_scan_bwd(const void *x, const void *delta,
+                                const void *Bt, const void *Ct,
+                                const float *A, const float *Dskip,
+                                const float *h0, const void *dy,
+                                const float *dh_last,
+                                void *dx, void *ddelta, float *dA,
+                                float *dBt, float *dCt, float *dDskip,
+                                float *dh0,
+                                int64_t B, int64_t L, int64_t D, int64_t N,
+                                int io_dtype, int delta_softplus,
+                                void *workspace, size_t workspace_bytes,
+                                void *stream);
+
 /* ------------------------------------------------------------ errors */
 
 /*

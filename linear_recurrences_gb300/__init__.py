@@ -27,7 +27,8 @@ __all__ = [
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
-    "ss_selective_scan_fwd_state", "new_workspace", "EXPORTED_SYMBOLS",
+    "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
+    "new_workspace", "EXPORTED_SYMBOLS",
 ]
 
 SS_OK, SS_ERR_INVALID, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -39,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_selective_scan_fwd_state",
+    "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
 )
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -101,6 +103,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_selective_scan_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                               i64, ci, ci, vp, sz, vp]
     L.ss_selective_scan_fwd_state.restype = ci
+    L.ss_selective_scan_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64]
+    L.ss_selective_scan_bwd_workspace_bytes.restype = sz
+    L.ss_selective_scan_bwd.argtypes = [vp] * 16 + [i64, i64, i64, i64, ci, ci, vp, sz, vp]
+    L.ss_selective_scan_bwd.restype = ci
     return L
 
 
@@ -321,3 +327,50 @@ def ss_get_device_status(workspace, stream=None) -> int:
     dev = workspace.device if workspace is not None else None
     sh = _stream_handle(stream, dev)
     return lib().ss_get_device_status(_ptr(workspace), sh)
+
+
+def ss_selective_scan_bwd_workspace_bytes(B, L, D, N) -> int:
+    return lib().ss_selective_scan_bwd_workspace_bytes(int(B), int(L), int(D), int(N))
+
+
+def ss_selective_scan_bwd(x, delta, Bt, Ct, A, Dskip, dy, h0=None, dh_last=None,
+                          delta_softplus=False, workspace=None, stream=None) -> dict:
+    """Gradients of sum(dy * y) + sum(dh_last * h_last) for
+    ss_selective_scan_fwd_state: dict with dx, ddelta (x's dtype), dA, dBt,
+    dCt, dDskip, dh0 (fp32)."""
+    torch = _torch()
+    io = (torch.float32, torch.bfloat16)
+    for t, nm in ((x, "x"), (delta, "delta"), (Bt, "Bt"), (Ct, "Ct"), (dy, "dy")):
+        _check_cuda(t, nm, io)
+    if not (x.dtype == delta.dtype == Bt.dtype == Ct.dtype == dy.dtype):
+        raise TypeError("x, delta, Bt, Ct, dy must share one dtype")
+    _check_cuda(A, "A", (torch.float32,))
+    B, L, D = x.shape
+    N = A.shape[1]
+    if delta.shape != x.shape or dy.shape != x.shape or Bt.shape != (B, L, N) or \
+            Ct.shape != (B, L, N) or A.shape != (D, N):
+        raise ValueError("shape mismatch between x, delta, dy, Bt, Ct, A")
+    for t, nm, shape in ((Dskip, "Dskip", (D,)), (h0, "h0", (B, D, N)),
+                         (dh_last, "dh_last", (B, D, N))):
+        if t is not None:
+            _check_cuda(t, nm, (torch.float32,))
+            if tuple(t.shape) != shape:
+                raise ValueError(f"{nm} must be {shape}")
+    dev = x.device
+    f32 = lambda *sh: torch.empty(sh, dtype=torch.float32, device=dev)
+    out = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x), "dA": f32(D, N),
+           "dBt": f32(B, L, N), "dCt": f32(B, L, N), "dDskip": f32(D), "dh0": f32(B, D, N)}
+    io_dtype = SS_BF16 if x.dtype == torch.bfloat16 else SS_F32
+    sh = _stream_handle(stream, dev)
+    need = ss_selective_scan_bwd_workspace_bytes(B, L, D, N)
+    if workspace is None and need:
+        workspace = _cached_workspace(("ss_selective_scan_bwd", B, L, D, N, need), need, dev, sh)
+    wsb = workspace.numel() if workspace is not None else 0
+    st = lib().ss_selective_scan_bwd(
+        _ptr(x), _ptr(delta), _ptr(Bt), _ptr(Ct), _ptr(A), _ptr(Dskip), _ptr(h0), _ptr(dy),
+        _ptr(dh_last), _ptr(out["dx"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dBt"]),
+        _ptr(out["dCt"]), _ptr(out["dDskip"]), _ptr(out["dh0"]), B, L, D, N, io_dtype,
+        int(bool(delta_softplus)), _ptr(workspace), wsb, sh)
+    if st != SS_OK:
+        raise SSError(st, "ss_selective_scan_bwd")
+    return out

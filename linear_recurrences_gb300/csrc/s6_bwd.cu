@@ -1,0 +1,535 @@
+// Backward pass of the S6 selective scan (sm_103a).
+//
+// The forward pass ("POPCORNBENCH FW-GLM-5-1 l2_p30", forward-pass
+// derivation) is, per channel (b, d) and state n,
+//   dl_t = softplus(v_t) or v_t,  dA_t = exp(dl_t A),  u_t = dl_t B_t x_t,
+//   h_t = dA_t h_{t-1} + u_t  (h_{-1} = h0),   y_t = sum_n C_t h_t + D x_t.
+// Its exact derivative for the loss sum dy*y + sum dh_last*h_last needs the
+// state h and the adjoint lam (the whole gradient of h_t) at the same t:
+//   lam_t = dy_t C_t + mu_{t+1},  mu_t = dA_t lam_t  (mu_L = dh_last),
+//   dC_t += dy_t h_t,  dB_t += lam_t dl_t x_t,  dx_t = D dy_t + sum lam dl B,
+//   ddl_t = sum_n lam_t (B_t x_t + A (h_t - u_t)),  dA += lam (h_t - u_t) dl,
+//   dh0 = mu_0,  and ddelta = ddl * sigmoid(v) under softplus.
+// (h_t - u_t = dA_t h_{t-1}, so no earlier state is needed.)
+//
+// Layout: time-parallel. A warp owns one channel of a 256-step chunk, lane l
+// the 8 consecutive steps 8l .. 8l+7, and loops over the states n; h and mu
+// for one n are warp scans (ordered shuffles) over the lanes' local affine
+// maps, so no per-(t, n) tensor is stored. Four launches:
+//   1. chunk aggregates (prod dA, forward end state from 0, adjoint entry
+//      from 0) per (b, chunk, d, n);
+//   2. carries: one thread per (b, d, n) walks the chunks forward (state
+//      entering each chunk, from h0) and backward (adjoint leaving each
+//      chunk, from dh_last; dh0 at the end);
+//   3. gradients per chunk: warps of 8 consecutive channels in lockstep;
+//      dB and dC, sums over d, go through shared memory in warp order into
+//      per-CTA sums over the CTA's channel range;
+//   4. fixed-order sums: dB, dC over the channel ranges; dA, dD over (b,
+//      chunk).
+// Every reduction has a fixed order, so results are bitwise reproducible.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "ss_common.cuh"
+#include "ss_internal.h"
+
+namespace ss {
+namespace {
+
+constexpr int kItems = 8;               // steps per lane
+constexpr int kChunk = 32 * kItems;     // steps per chunk
+constexpr int kWarps = 8;               // channels in flight per CTA
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxN = 16;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct BwdParams {
+    const void *x, *delta, *Bt, *Ct, *dy;
+    const float *A, *Dskip, *h0, *dh_last;
+    void *dx, *ddelta;
+    float *dA, *dBt, *dCt, *dDskip, *dh0;
+    long long B, L, D;
+    int N;
+    int K;           // chunks per sequence
+    int SD;          // channel ranges (CTAs per (b, chunk))
+    int Dr;          // channels per range (multiple of kWarps)
+    int softplus;
+    // workspace, each [B][K][D][N] unless noted
+    float *aggP, *aggH, *aggM;   // chunk aggregates
+    float *carH, *carM;          // state entering / adjoint leaving each chunk
+    float *partA;                // dA partial per (b, chunk)
+    float *partD;                // [B][K][D] dDskip partial per (b, chunk)
+    float *partB, *partC;        // [SD][B][L][N] dB, dC partial per channel range
+};
+
+__device__ __forceinline__ float ld_io(const float *p, long long i) { return __ldg(p + i); }
+__device__ __forceinline__ float ld_io(const __nv_bfloat16 *p, long long i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_io(float *p, long long i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_io(__nv_bfloat16 *p, long long i, float v) {
+    p[i] = __float2bfloat16_rn(v);
+}
+
+// softplus(v) = log(1 + exp(v)), v > 20 passes through; the same MUFU form,
+// with the series for small exp(v), as the forward kernels use.
+__device__ __forceinline__ float softplus_fwd(float v) {
+    const float e = ex2_approx(fminf(v, 20.0f) * kLog2e);
+    const float series = e * (1.0f - e * (0.5f - e * (1.0f / 3.0f - 0.25f * e)));
+    const float logged = lg2_approx(1.0f + e) * kLn2;
+    const float r = e < 0.015625f ? series : logged;
+    return v > 20.0f ? v : r;
+}
+// d softplus / dv = sigmoid(v); 1 above the pass-through threshold.
+__device__ __forceinline__ float softplus_grad(float v) {
+    return v > 20.0f ? 1.0f : 1.0f / (1.0f + ex2_approx(-v * kLog2e));
+}
+
+struct Map {  // x -> a x + b
+    float a, b;
+};
+// p then q (p earlier in time for the forward state, the reverse order for
+// the adjoint: the caller passes the map applied first as p).
+__device__ __forceinline__ Map then(Map p, Map q) { return {p.a * q.a, fmaf(q.a, p.b, q.b)}; }
+
+// Exclusive scan over lanes of maps applied in lane order (lane 0 first):
+// returns the composition of lanes 0 .. l-1 (identity for lane 0).
+__device__ __forceinline__ Map warp_exclusive_fwd(Map m, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float a = __shfl_up_sync(kFull, m.a, off);
+        const float b = __shfl_up_sync(kFull, m.b, off);
+        if (lane >= off) m = then({a, b}, m);
+    }
+    Map e;
+    e.a = __shfl_up_sync(kFull, m.a, 1);
+    e.b = __shfl_up_sync(kFull, m.b, 1);
+    if (lane == 0) e = {1.0f, 0.0f};
+    return e;
+}
+// Exclusive scan over lanes of maps applied in reverse lane order (lane 31
+// first): returns the composition of lanes 31 .. l+1 (identity for lane 31).
+__device__ __forceinline__ Map warp_exclusive_rev(Map m, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float a = __shfl_down_sync(kFull, m.a, off);
+        const float b = __shfl_down_sync(kFull, m.b, off);
+        if (lane + off < 32) m = then({a, b}, m);
+    }
+    Map e;
+    e.a = __shfl_down_sync(kFull, m.a, 1);
+    e.b = __shfl_down_sync(kFull, m.b, 1);
+    if (lane == 31) e = {1.0f, 0.0f};
+    return e;
+}
+// Sum over lanes in a fixed tree order (lane 0's result is used).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+    return v;
+}
+// Composition of all 32 lanes' maps in lane order (lane 0 first); lane 0
+// holds the result.
+__device__ __forceinline__ Map warp_total_fwd(Map m, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float a = __shfl_down_sync(kFull, m.a, off);
+        const float b = __shfl_down_sync(kFull, m.b, off);
+        if (lane + off < 32) m = then(m, {a, b});
+    }
+    return m;
+}
+// Composition in reverse lane order (lane 31 first); lane 0 holds it.
+__device__ __forceinline__ Map warp_total_rev(Map m, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float a = __shfl_down_sync(kFull, m.a, off);
+        const float b = __shfl_down_sync(kFull, m.b, off);
+        if (lane + off < 32) m = then({a, b}, m);
+    }
+    return m;
+}
+
+// One CTA: chunk k of batch b, channel range r. Shared Bt / Ct tiles of the
+// chunk laid out [n][item][lane], so lane reads are conflict-free.
+struct ChunkCtx {
+    long long b, t0;
+    int k, d0, d1;  // channels [d0, d1)
+};
+__device__ __forceinline__ ChunkCtx chunk_ctx(const BwdParams &p) {
+    ChunkCtx c;
+    const long long bk = blockIdx.x / p.SD;
+    const int r = (int)(blockIdx.x % p.SD);
+    c.b = bk / p.K;
+    c.k = (int)(bk % p.K);
+    c.t0 = (long long)c.k * kChunk;
+    c.d0 = r * p.Dr;
+    c.d1 = (int)min((long long)(c.d0 + p.Dr), p.D);
+    return c;
+}
+__device__ __forceinline__ void load_bc_tiles(const BwdParams &p, const ChunkCtx &c, float *Bs,
+                                              float *Cs, bool bf16) {
+    const int N = p.N;
+    for (int idx = threadIdx.x; idx < kChunk * N; idx += kThreads) {
+        const int tl = idx / N, n = idx - tl * N;
+        const long long t = c.t0 + tl;
+        float bv = 0.0f, cv = 0.0f;
+        if (t < p.L) {
+            const long long g = (c.b * p.L + t) * N + n;
+            if (bf16) {
+                bv = ld_io(static_cast<const __nv_bfloat16 *>(p.Bt), g);
+                cv = ld_io(static_cast<const __nv_bfloat16 *>(p.Ct), g);
+            } else {
+                bv = ld_io(static_cast<const float *>(p.Bt), g);
+                cv = ld_io(static_cast<const float *>(p.Ct), g);
+            }
+        }
+        const int s = n * kChunk + (tl & (kItems - 1)) * 32 + tl / kItems;  // [n][item][lane]
+        Bs[s] = bv;
+        Cs[s] = cv;
+    }
+}
+
+// This lane's 8 steps of channel d: discretisation step, x and dy (zeros for
+// steps past L or an absent channel, which makes every map the identity).
+template <typename IO>
+__device__ __forceinline__ void load_items(const BwdParams &p, const ChunkCtx &c, int d, bool dok,
+                                           int lane, float (&dl)[kItems], float (&x)[kItems],
+                                           float (&gy)[kItems], float (&v)[kItems]) {
+    const IO *xp = static_cast<const IO *>(p.x);
+    const IO *dp = static_cast<const IO *>(p.delta);
+    const IO *yp = static_cast<const IO *>(p.dy);
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        const long long t = c.t0 + lane * kItems + i;
+        dl[i] = x[i] = gy[i] = v[i] = 0.0f;
+        if (dok && t < p.L) {
+            const long long g = (c.b * p.L + t) * p.D + d;
+            v[i] = ld_io(dp, g);
+            dl[i] = p.softplus ? softplus_fwd(v[i]) : v[i];
+            x[i] = ld_io(xp, g);
+            gy[i] = ld_io(yp, g);
+        }
+    }
+}
+
+// ---- launch 1: per (b, chunk, d, n) the product of dA, the forward end
+// state from zero, and the adjoint entering the chunk from zero.
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) bwd_aggregate_kernel(const BwdParams p) {
+    __shared__ float Bs[kMaxN * kChunk], Cs[kMaxN * kChunk];
+    const ChunkCtx c = chunk_ctx(p);
+    load_bc_tiles(p, c, Bs, Cs, sizeof(IO) == 2);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int d = c.d0 + warp; d < c.d1; d += kWarps) {
+        float dl[kItems], x[kItems], gy[kItems], v[kItems];
+        load_items<IO>(p, c, d, true, lane, dl, x, gy, v);
+        for (int n = 0; n < p.N; ++n) {
+            const float A2 = p.A[(long long)d * p.N + n] * kLog2e;
+            float dA[kItems];
+            Map f = {1.0f, 0.0f};
+#pragma unroll
+            for (int i = 0; i < kItems; ++i) {
+                dA[i] = ex2_approx(dl[i] * A2);
+                const float u = dl[i] * (x[i] * Bs[n * kChunk + i * 32 + lane]);
+                f = {f.a * dA[i], fmaf(dA[i], f.b, u)};
+            }
+            Map r = {1.0f, 0.0f};  // adjoint: mu_in -> r.a mu_in + r.b
+#pragma unroll
+            for (int i = kItems - 1; i >= 0; --i) {
+                const float g = gy[i] * Cs[n * kChunk + i * 32 + lane];
+                r = {r.a * dA[i], dA[i] * (g + r.b)};
+            }
+            f = warp_total_fwd(f, lane);
+            r = warp_total_rev(r, lane);
+            if (lane == 0) {
+                const long long idx = ((c.b * p.K + c.k) * p.D + d) * p.N + n;
+                p.aggP[idx] = f.a;
+                p.aggH[idx] = f.b;
+                p.aggM[idx] = r.b;
+            }
+        }
+    }
+}
+
+// ---- launch 2: per (b, d, n), the state entering each chunk (from h0) and
+// the adjoint leaving each chunk (from dh_last), chunk by chunk in order;
+// dh0 is the adjoint left at the sequence's start.
+__global__ void bwd_carry_kernel(const BwdParams p) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long total = p.B * p.D * p.N;
+    if (i >= total) return;
+    const long long b = i / (p.D * p.N), dn = i - b * p.D * p.N;  // dn = d*N + n
+    const long long stride = p.D * p.N;
+    const long long base = b * p.K * stride + dn;
+    float h = p.h0 ? p.h0[i] : 0.0f;
+    for (int k = 0; k < p.K; ++k) {
+        const long long idx = base + k * stride;
+        p.carH[idx] = h;
+        h = fmaf(p.aggP[idx], h, p.aggH[idx]);
+    }
+    float mu = p.dh_last ? p.dh_last[i] : 0.0f;
+    for (int k = p.K - 1; k >= 0; --k) {
+        const long long idx = base + k * stride;
+        p.carM[idx] = mu;
+        mu = fmaf(p.aggP[idx], mu, p.aggM[idx]);
+    }
+    if (p.dh0) p.dh0[i] = mu;
+}
+
+constexpr int kGradSmem = (4 * kMaxN + 2 * kWarps) * kChunk * (int)sizeof(float);  // 80 KB
+
+// ---- launch 3: gradients of one chunk for a channel range. Warp w takes
+// channels d0 + w, d0 + w + 8, ...; per state n each warp rebuilds h over its
+// steps (warp scan from the chunk's entering state) and runs the adjoint
+// back over them (warp scan from the chunk's leaving adjoint), accumulating
+// the per-step terms. dB and dC contributions of the 8 warps meet in shared
+// memory and are added in warp order; the CTA's channel-range sums are
+// written once at the end.
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
+    extern __shared__ __align__(16) float smem[];  // kGradSmem bytes
+    float *Bs = smem, *Cs = Bs + kMaxN * kChunk;
+    float *accB = Cs + kMaxN * kChunk, *accC = accB + kMaxN * kChunk;  // [n][item][lane]
+    float *redB = accC + kMaxN * kChunk, *redC = redB + kWarps * kChunk;  // [warp][item][lane]
+    const ChunkCtx c = chunk_ctx(p);
+    load_bc_tiles(p, c, Bs, Cs, sizeof(IO) == 2);
+    for (int i = threadIdx.x; i < kMaxN * kChunk; i += kThreads) accB[i] = accC[i] = 0.0f;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int N = p.N;
+    IO *dxp = static_cast<IO *>(p.dx);
+    IO *ddp = static_cast<IO *>(p.ddelta);
+
+    for (int dbase = c.d0; dbase < c.d1; dbase += kWarps) {
+        const int d = dbase + warp;
+        const bool dok = d < c.d1;  // warp-uniform; absent channels add zeros
+        float dl[kItems], x[kItems], gy[kItems], v[kItems];
+        load_items<IO>(p, c, d, dok, lane, dl, x, gy, v);
+        float gdl[kItems], gx[kItems];
+#pragma unroll
+        for (int i = 0; i < kItems; ++i) gdl[i] = gx[i] = 0.0f;
+
+        for (int n = 0; n < N; ++n) {
+            const long long cidx = ((c.b * p.K + c.k) * p.D + d) * N + n;
+            const float An = dok ? p.A[(long long)d * N + n] : 0.0f;
+            const float A2 = An * kLog2e;
+            const float hs = dok ? p.carH[cidx] : 0.0f;  // state entering the chunk
+            const float me = dok ? p.carM[cidx] : 0.0f;  // adjoint leaving it
+            float dA[kItems], u[kItems], g[kItems], h[kItems];
+            Map f = {1.0f, 0.0f};
+#pragma unroll
+            for (int i = 0; i < kItems; ++i) {
+                dA[i] = ex2_approx(dl[i] * A2);
+                u[i] = dl[i] * (x[i] * Bs[n * kChunk + i * 32 + lane]);
+                g[i] = gy[i] * Cs[n * kChunk + i * 32 + lane];
+                f = {f.a * dA[i], fmaf(dA[i], f.b, u[i])};
+            }
+            const Map ef = warp_exclusive_fwd(f, lane);
+            const float s = fmaf(ef.a, hs, ef.b);  // state before this lane's first step
+            float hc = s;
+#pragma unroll
+            for (int i = 0; i < kItems; ++i) h[i] = hc = fmaf(dA[i], hc, u[i]);
+            Map r = {1.0f, 0.0f};
+#pragma unroll
+            for (int i = kItems - 1; i >= 0; --i) r = {r.a * dA[i], dA[i] * (g[i] + r.b)};
+            const Map er = warp_exclusive_rev(r, lane);
+            float mu = fmaf(er.a, me, er.b);  // adjoint after this lane's last step
+            float dAp = 0.0f;
+#pragma unroll
+            for (int i = kItems - 1; i >= 0; --i) {
+                const float lam = g[i] + mu;                      // gradient of h_t
+                const float hprev = i > 0 ? h[i - 1] : s;
+                const float tA = lam * (dA[i] * hprev);           // through dA_t
+                const float Bv = Bs[n * kChunk + i * 32 + lane];
+                gdl[i] = fmaf(lam, Bv * x[i], gdl[i]);
+                gdl[i] = fmaf(tA, An, gdl[i]);
+                gx[i] = fmaf(lam, dl[i] * Bv, gx[i]);
+                dAp = fmaf(tA, dl[i], dAp);
+                redB[warp * kChunk + i * 32 + lane] = lam * (dl[i] * x[i]);
+                redC[warp * kChunk + i * 32 + lane] = gy[i] * h[i];
+                mu = dA[i] * lam;
+            }
+            dAp = warp_sum(dAp);
+            if (dok && lane == 0) p.partA[cidx] = dAp;
+            __syncthreads();
+            // this chunk's dB, dC for state n: the 8 warps' terms in warp order
+            {
+                const int j = threadIdx.x;  // [item][lane] position
+                float sb = accB[n * kChunk + j], sc = accC[n * kChunk + j];
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    sb += redB[w * kChunk + j];
+                    sc += redC[w * kChunk + j];
+                }
+                accB[n * kChunk + j] = sb;
+                accC[n * kChunk + j] = sc;
+            }
+            __syncthreads();
+        }
+        if (dok) {
+            const float Dd = p.Dskip ? p.Dskip[d] : 0.0f;
+            float sdx = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kItems; ++i) {
+                const long long t = c.t0 + lane * kItems + i;
+                sdx = fmaf(gy[i], x[i], sdx);
+                if (t < p.L) {
+                    const long long gidx = (c.b * p.L + t) * p.D + d;
+                    st_io(dxp, gidx, fmaf(gy[i], Dd, gx[i]));
+                    st_io(ddp, gidx, p.softplus ? gdl[i] * softplus_grad(v[i]) : gdl[i]);
+                }
+            }
+            sdx = warp_sum(sdx);
+            if (lane == 0) p.partD[(c.b * p.K + c.k) * p.D + d] = sdx;
+        }
+    }
+    // this channel range's dB, dC over the chunk
+    const int r = (int)(blockIdx.x % p.SD);
+    for (int idx = threadIdx.x; idx < N * kChunk; idx += kThreads) {
+        const int n = idx / kChunk, j = idx - n * kChunk;
+        const int tl = (j & 31) * kItems + (j >> 5);  // lane * 8 + item
+        const long long t = c.t0 + tl;
+        if (t < p.L) {
+            const long long o = (((long long)r * p.B + c.b) * p.L + t) * N + n;
+            p.partB[o] = accB[idx];
+            p.partC[o] = accC[idx];
+        }
+    }
+}
+
+// ---- launch 4: the remaining sums, each in a fixed order: dBt, dCt over
+// the channel ranges; dA and dDskip over (b, chunk).
+__global__ void bwd_final_kernel(const BwdParams p) {
+    const long long nBC = p.B * p.L * p.N, nA = p.D * p.N, nD = p.dDskip ? p.D : 0;
+    const long long total = nBC + nA + nD;
+    const long long BK = p.B * p.K;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        if (i < nBC) {
+            float sb = 0.0f, sc = 0.0f;
+            for (int r = 0; r < p.SD; ++r) {
+                sb += p.partB[(long long)r * nBC + i];
+                sc += p.partC[(long long)r * nBC + i];
+            }
+            p.dBt[i] = sb;
+            p.dCt[i] = sc;
+        } else if (i < nBC + nA) {
+            const long long dn = i - nBC;
+            float s = 0.0f;
+            for (long long bk = 0; bk < BK; ++bk) s += p.partA[bk * nA + dn];
+            p.dA[dn] = s;
+        } else {
+            const long long d = i - nBC - nA;
+            float s = 0.0f;
+            for (long long bk = 0; bk < BK; ++bk) s += p.partD[bk * p.D + d];
+            p.dDskip[d] = s;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ planning
+struct BwdPlan {
+    int K, SD, Dr;
+    size_t off[9];  // section offsets: aggP aggH aggM carH carM partA partD partB partC
+    size_t total;
+};
+
+int sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return sms;
+}
+
+BwdPlan bwd_plan(int64_t B, int64_t L, int64_t D, int64_t N) {
+    BwdPlan pl{};
+    pl.K = (int)((L + kChunk - 1) / kChunk);
+    // enough CTAs for about four per SM, splitting the channels into ranges
+    const long long target = (long long)sm_count() * 4;
+    const long long groups = (D + kWarps - 1) / kWarps;
+    long long SD = (target + B * pl.K - 1) / std::max<long long>(B * pl.K, 1);
+    SD = std::max<long long>(1, std::min<long long>(SD, groups));
+    pl.Dr = (int)(((groups + SD - 1) / SD) * kWarps);
+    pl.SD = (int)((D + pl.Dr - 1) / pl.Dr);
+    const size_t bkdn = (size_t)B * pl.K * D * N * sizeof(float);
+    const size_t sizes[9] = {bkdn, bkdn, bkdn, bkdn, bkdn, bkdn,
+                             (size_t)B * pl.K * D * sizeof(float),
+                             (size_t)pl.SD * B * L * N * sizeof(float),
+                             (size_t)pl.SD * B * L * N * sizeof(float)};
+    size_t o = 0;
+    for (int i = 0; i < 9; ++i) {
+        pl.off[i] = o;
+        o += (sizes[i] + 255) / 256 * 256;
+    }
+    pl.total = o;
+    return pl;
+}
+
+}  // namespace
+
+size_t s6_bwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
+    if (B <= 0 || L <= 0 || D <= 0 || N <= 0) return 0;
+    return bwd_plan(B, L, D, N).total;
+}
+
+ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    const BwdPlan pl = bwd_plan(a.B, a.L, a.D, a.N);
+    if (workspace == nullptr || ws_bytes < pl.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return SS_ERR_WORKSPACE;
+    BwdParams p{};
+    p.x = a.x;
+    p.delta = a.delta;
+    p.Bt = a.Bt;
+    p.Ct = a.Ct;
+    p.dy = a.dy;
+    p.A = a.A;
+    p.Dskip = a.Dskip;
+    p.h0 = a.h0;
+    p.dh_last = a.dh_last;
+    p.dx = a.dx;
+    p.ddelta = a.ddelta;
+    p.dA = a.dA;
+    p.dBt = a.dBt;
+    p.dCt = a.dCt;
+    p.dDskip = a.dDskip;
+    p.dh0 = a.dh0;
+    p.B = a.B;
+    p.L = a.L;
+    p.D = a.D;
+    p.N = (int)a.N;
+    p.K = pl.K;
+    p.SD = pl.SD;
+    p.Dr = pl.Dr;
+    p.softplus = a.softplus;
+    char *ws = static_cast<char *>(workspace);
+    float **sec[9] = {&p.aggP, &p.aggH, &p.aggM, &p.carH, &p.carM, &p.partA, &p.partD, &p.partB, &p.partC};
+    for (int i = 0; i < 9; ++i) *sec[i] = reinterpret_cast<float *>(ws + pl.off[i]);
+    const long long grid = a.B * pl.K * pl.SD;
+    if (grid > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
+    if (a.io_bf16)
+        bwd_aggregate_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, 0, stream>>>(p);
+    else
+        bwd_aggregate_kernel<float><<<(unsigned)grid, kThreads, 0, stream>>>(p);
+    const long long chains = a.B * a.D * a.N;
+    bwd_carry_kernel<<<(unsigned)((chains + 255) / 256), 256, 0, stream>>>(p);
+    auto grad = a.io_bf16 ? bwd_grad_kernel<__nv_bfloat16> : bwd_grad_kernel<float>;
+    if (cudaFuncSetAttribute(grad, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradSmem) !=
+        cudaSuccess)
+        return SS_ERR_CUDA;
+    grad<<<(unsigned)grid, kThreads, kGradSmem, stream>>>(p);
+    bwd_final_kernel<<<sm_count() * 8, 256, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace ss

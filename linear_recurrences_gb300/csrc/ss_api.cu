@@ -123,6 +123,75 @@ ss_status ss_selective_scan_fwd_state(const void *x, const void *delta, const vo
                     workspace_bytes, stream, 0, h0, h_last);
 }
 
+size_t ss_selective_scan_bwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
+    if (N < 1 || N > 16) return 0;
+    return ss::s6_bwd_workspace_bytes(B, L, D, N);
+}
+
+ss_status ss_selective_scan_bwd(const void *x, const void *delta, const void *Bt, const void *Ct,
+                                const float *A, const float *Dskip, const float *h0, const void *dy,
+                                const float *dh_last, void *dx, void *ddelta, float *dA,
+                                float *dBt, float *dCt, float *dDskip, float *dh0, int64_t B,
+                                int64_t L, int64_t D, int64_t N, int io_dtype, int delta_softplus,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || L < 0 || D < 0 || N < 0) return SS_ERR_INVALID;
+    if (io_dtype != SS_F32 && io_dtype != SS_BF16) return SS_ERR_INVALID;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    if (B > (1LL << 31) || L > (1LL << 40) || D > (1LL << 31) || B * L > (1LL << 48))
+        return SS_ERR_UNSUPPORTED;
+    const uintptr_t es = io_dtype == SS_BF16 ? 2 : 4;
+    const bool empty = B == 0 || L == 0 || D == 0;
+    if (!A || !dA || (!empty && (!x || !delta || !Bt || !Ct || !dy || !dx || !ddelta)) ||
+        (B * L > 0 && (!dBt || !dCt)))
+        return SS_ERR_INVALID;
+    if (!aligned(x, es) || !aligned(delta, es) || !aligned(Bt, es) || !aligned(Ct, es) ||
+        !aligned(dy, es) || !aligned(dx, es) || !aligned(ddelta, es) || !aligned(A, 4) ||
+        !aligned(Dskip, 4) || !aligned(h0, 4) || !aligned(dh_last, 4) || !aligned(dA, 4) ||
+        !aligned(dBt, 4) || !aligned(dCt, 4) || !aligned(dDskip, 4) || !aligned(dh0, 4))
+        return SS_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (empty) {
+        // sums over nothing are zero; with no steps h_last is h0, so dh0 = dh_last
+        bool ok = cudaMemsetAsync(dA, 0, (size_t)(D * N) * sizeof(float), s) == cudaSuccess;
+        if (dDskip) ok &= cudaMemsetAsync(dDskip, 0, (size_t)D * sizeof(float), s) == cudaSuccess;
+        if (B * L > 0) {
+            ok &= cudaMemsetAsync(dBt, 0, (size_t)(B * L * N) * sizeof(float), s) == cudaSuccess;
+            ok &= cudaMemsetAsync(dCt, 0, (size_t)(B * L * N) * sizeof(float), s) == cudaSuccess;
+        }
+        if (dh0 && B * D > 0) {
+            const size_t bytes = (size_t)(B * D * N) * sizeof(float);
+            ok &= (dh_last && L == 0
+                       ? cudaMemcpyAsync(dh0, dh_last, bytes, cudaMemcpyDeviceToDevice, s)
+                       : cudaMemsetAsync(dh0, 0, bytes, s)) == cudaSuccess;
+        }
+        return ok ? SS_OK : SS_ERR_CUDA;
+    }
+    ss::S6BwdArgs a;
+    a.x = x;
+    a.delta = delta;
+    a.Bt = Bt;
+    a.Ct = Ct;
+    a.dy = dy;
+    a.A = A;
+    a.Dskip = Dskip;
+    a.h0 = h0;
+    a.dh_last = dh_last;
+    a.dx = dx;
+    a.ddelta = ddelta;
+    a.dA = dA;
+    a.dBt = dBt;
+    a.dCt = dCt;
+    a.dDskip = dDskip;
+    a.dh0 = dh0;
+    a.B = B;
+    a.L = L;
+    a.D = D;
+    a.N = N;
+    a.io_bf16 = io_dtype == SS_BF16;
+    a.softplus = delta_softplus != 0;
+    return ss::s6_bwd_launch(a, workspace, workspace_bytes, s);
+}
+
 ss_status ss_get_device_status(void *workspace, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(s) != cudaSuccess) return SS_ERR_CUDA;

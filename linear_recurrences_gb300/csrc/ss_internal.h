@@ -29,6 +29,18 @@ struct S6Args {
 unsigned long long spin_timeout_ns();
 
 size_t s6_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir);
+
+struct S6BwdArgs {
+    const void *x, *delta, *Bt, *Ct, *dy;
+    const float *A, *Dskip, *h0, *dh_last;
+    void *dx, *ddelta;
+    float *dA, *dBt, *dCt, *dDskip, *dh0;
+    int64_t B, L, D, N;
+    int io_bf16;
+    int softplus;
+};
+size_t s6_bwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N);
+ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream);
 ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStream_t stream,
                     unsigned long long timeout_ns, long long skip_unit);
 

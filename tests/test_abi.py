@@ -95,6 +95,29 @@ def test_s6_state_argument_errors(L):
     assert fn(*args(p, p, B=-1)) == ss.SS_ERR_INVALID
 
 
+def test_s6_bwd_argument_errors(L):
+    p = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(258)
+    fn = L.ss_selective_scan_bwd
+    # x delta Bt Ct A Dskip h0 dy dh_last dx ddelta dA dBt dCt dDskip dh0
+    args = lambda ptrs, B=2, L_=8, D=4, N=16, io=0: (*ptrs, B, L_, D, N, io, 0, p, 1 << 30, None)
+    full = [p] * 16
+    assert fn(*args(full, N=17)) == ss.SS_ERR_UNSUPPORTED
+    assert fn(*args(full, io=5)) == ss.SS_ERR_INVALID
+    assert fn(*args(full, B=-1)) == ss.SS_ERR_INVALID
+    for i in (0, 1, 2, 3, 4, 7, 9, 10, 11, 12, 13):  # required pointers
+        bad = list(full)
+        bad[i] = None
+        assert fn(*args(bad)) == ss.SS_ERR_INVALID, f"null argument {i} accepted"
+    for i in range(16):
+        bad = list(full)
+        bad[i] = odd
+        assert fn(*args(bad)) == ss.SS_ERR_INVALID, f"misaligned argument {i} accepted"
+    assert fn(*(full + [2, 8, 4, 16, 0, 0, None, 0, None])) == ss.SS_ERR_WORKSPACE
+    assert L.ss_selective_scan_bwd_workspace_bytes(2, 8, 4, 17) == 0
+    assert L.ss_selective_scan_bwd_workspace_bytes(0, 8, 4, 16) == 0
+
+
 def test_spin_timeout(L):
     assert L.ss_set_spin_timeout_ns(0) == ss.SS_ERR_INVALID
     assert L.ss_set_spin_timeout_ns(10**9) == ss.SS_OK
