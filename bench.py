@@ -225,14 +225,27 @@ def s6_bytes_and_ops(w):
     return byts, mufu
 
 
+def s6_variant(name):
+    """(workload, variant) for an S6 bench name: "s6_x", "s6_x_state" or
+    "s6_x_bwd"."""
+    import workloads
+    for suffix in ("_state", "_bwd"):
+        if name.endswith(suffix) and name[: -len(suffix)] in workloads.S6:
+            return workloads.S6[name[: -len(suffix)]], suffix[1:]
+    return workloads.S6[name], ""
+
+
 def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
-    """One S6 workload; a name ending in "_state" runs the forward-with-state
-    call on the workload before the suffix, from a seeded random h0 and
-    writing h_last (2 x B*D*N*4 more bytes)."""
+    """One S6 workload. A name ending in "_state" runs the forward-with-state
+    call from a seeded random h0, writing h_last (2 x B*D*N*4 more bytes); one
+    ending in "_bwd" runs the backward pass for a seeded random dy: reads x,
+    delta, dy, Bt, Ct once and writes dx, ddelta (storage type) and dBt, dCt,
+    dA, dDskip (fp32); MUFU ops BLDN + (3 BLD with softplus: softplus and its
+    sigmoid)."""
     import numpy as np
     import workloads
-    state = name.endswith("_state")
-    w = workloads.S6[name[: -len("_state")] if state else name]
+    w, variant = s6_variant(name)
+    state = variant == "state"
     inp = workloads.s6_workload_inputs(w)
 
     def t(v):
@@ -253,6 +266,18 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
         call = lambda: ss.ss_selective_scan_fwd_state(*args, h0=h0, delta_softplus=w.softplus,
                                                       y=y, h_last=h_last, stream=stream)
         byts += 2 * 4 * w.B * w.D * w.N
+    if variant == "bwd":
+        g = np.random.Generator(np.random.PCG64(17))
+        dy = t(g.standard_normal((w.B, w.L, w.D)).astype(np.float32))
+        if inp.io == "bf16":
+            dy = dy.to(torch.bfloat16)
+        ws = ss.new_workspace(ss.ss_selective_scan_bwd_workspace_bytes(w.B, w.L, w.D, w.N), dev)
+        call = lambda: ss.ss_selective_scan_bwd(*args, dy, delta_softplus=w.softplus,
+                                                workspace=ws, stream=stream)
+        es = 2 if w.io == "bf16" else 4
+        BLD, BLN = w.B * w.L * w.D, w.B * w.L * w.N
+        byts = 5 * es * BLD + 2 * es * BLN + 2 * 4 * BLN + 4 * (2 * w.D * w.N + 2 * w.D)
+        mufu = BLD * w.N + (3 * BLD if w.softplus else 0)
     flush = None
     if byts < 2 * L2_BYTES:
         junk = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
@@ -264,15 +289,19 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
     t_roof = max(t_hbm, t_sfu)
     return {
         "elements": w.elements, "shape": [w.B, w.L, w.D, w.N], "io": w.io,
-        "softplus": w.softplus, "bidir": w.bidir, "state": state, "ms": ms, "ms_min": min(per),
+        "softplus": w.softplus, "bidir": w.bidir, "variant": variant or "forward", "ms": ms,
+        "ms_min": min(per),
         "elements_per_s": w.elements / (ms * 1e-3),
         "gbs": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts, "mufu_ops": mufu,
         "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6,
         "bound": "hbm" if t_hbm >= t_sfu else "sfu",
         "roofline_frac": t_roof / (ms * 1e-3),
         "l2": "flushed between calls" if flush else "inputs larger than L2",
-        "workspace_bytes": ss.ss_selective_scan_workspace_bytes(
-            w.B, w.L, w.D, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32, w.bidir),
+        "workspace_bytes": (
+            ss.ss_selective_scan_bwd_workspace_bytes(w.B, w.L, w.D, w.N) if variant == "bwd" else
+            ss.ss_selective_scan_workspace_bytes(w.B, w.L, w.D, w.N,
+                                                 ss.SS_BF16 if w.io == "bf16" else ss.SS_F32,
+                                                 w.bidir)),
     }
 
 
@@ -405,7 +434,8 @@ def run_ours(args, rank, world, local_rank):
         per_cfg[HEADLINE] = {"elements": w.n, "ms": launch_ms,
                              "elements_per_s": w.n / (launch_ms * 1e-3), "gbs": achieved,
                              "bound": "hbm", "roofline_frac": achieved / hbm_peak}
-        for name in ("s6_fp32", "s6_bf16", "s6_bidir", "s6_bf16_state"):
+        for name in ("s6_fp32", "s6_bf16", "s6_bidir", "s6_bf16_state", "s6_fp32_bwd",
+                     "s6_bf16_bwd"):
             per_cfg[name] = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream,
                                      hbm_peak, sfu)
         extras["per_config"] = per_cfg
@@ -449,7 +479,8 @@ def run_single(args):
     peaks, _ = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     name = args.workload
-    if name in workloads.S6 or (name.endswith("_state") and name[:-6] in workloads.S6):
+    if name in workloads.S6 or any(name.endswith(x) and name[: -len(x)] in workloads.S6
+                                   for x in ("_state", "_bwd")):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         sfu = mufu_probe(torch, ss, dev, sms) if not args.no_extras else 9.86e12
         r = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream, hbm_peak, sfu)
@@ -482,7 +513,8 @@ def main():
                     help="with --workload affine_*: use this many elements (small ncu captures)")
     ap.add_argument("--workload", default=HEADLINE,
                     help="time one workload only (affine_small, affine_large, s6_fp32, "
-                         "s6_bf16, s6_bidir, s6_bf16_state); the default is the full benchmark")
+                         "s6_bf16, s6_bidir, s6_bf16_state, s6_fp32_bwd, s6_bf16_bwd); the default "
+                         "is the full benchmark")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -222,31 +222,32 @@ __device__ __forceinline__ void load_items(const BwdParams &p, const ChunkCtx &c
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) bwd_aggregate_kernel(const BwdParams p) {
     __shared__ float Bs[kMaxN * kChunk], Cs[kMaxN * kChunk];
+    __shared__ float sA[kWarps][kMaxN];
     const ChunkCtx c = chunk_ctx(p);
     load_bc_tiles(p, c, Bs, Cs, sizeof(IO) == 2);
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int d = c.d0 + warp; d < c.d1; d += kWarps) {
+        if (lane < p.N) sA[warp][lane] = p.A[(long long)d * p.N + lane] * kLog2e;
         float dl[kItems], x[kItems], gy[kItems], v[kItems];
         load_items<IO>(p, c, d, true, lane, dl, x, gy, v);
+#pragma unroll
+        for (int i = 0; i < kItems; ++i) x[i] *= dl[i];  // x now holds dl * x
+        __syncwarp();
         for (int n = 0; n < p.N; ++n) {
-            const float A2 = p.A[(long long)d * p.N + n] * kLog2e;
+            const float A2 = sA[warp][n];
             float dA[kItems];
             Map f = {1.0f, 0.0f};
 #pragma unroll
             for (int i = 0; i < kItems; ++i) {
                 dA[i] = ex2_approx(dl[i] * A2);
-                const float u = dl[i] * (x[i] * Bs[n * kChunk + i * 32 + lane]);
-                f = {f.a * dA[i], fmaf(dA[i], f.b, u)};
+                f = {f.a * dA[i], fmaf(dA[i], f.b, x[i] * Bs[n * kChunk + i * 32 + lane])};
             }
-            Map r = {1.0f, 0.0f};  // adjoint: mu_in -> r.a mu_in + r.b
+            float m = 0.0f;  // adjoint: mu_in -> f.a mu_in + m
 #pragma unroll
-            for (int i = kItems - 1; i >= 0; --i) {
-                const float g = gy[i] * Cs[n * kChunk + i * 32 + lane];
-                r = {r.a * dA[i], dA[i] * (g + r.b)};
-            }
+            for (int i = kItems - 1; i >= 0; --i) m = dA[i] * (gy[i] * Cs[n * kChunk + i * 32 + lane] + m);
+            const Map r = warp_total_rev({f.a, m}, lane);
             f = warp_total_fwd(f, lane);
-            r = warp_total_rev(r, lane);
             if (lane == 0) {
                 const long long idx = ((c.b * p.K + c.k) * p.D + d) * p.N + n;
                 p.aggP[idx] = f.a;
@@ -254,6 +255,7 @@ __global__ void __launch_bounds__(kThreads) bwd_aggregate_kernel(const BwdParams
                 p.aggM[idx] = r.b;
             }
         }
+        __syncwarp();  // sA is rewritten for the next channel
     }
 }
 
@@ -282,7 +284,8 @@ __global__ void bwd_carry_kernel(const BwdParams p) {
     if (p.dh0) p.dh0[i] = mu;
 }
 
-constexpr int kGradSmem = (4 * kMaxN + 2 * kWarps) * kChunk * (int)sizeof(float);  // 80 KB
+constexpr int kGradSmem =
+    ((4 * kMaxN + 2 * kWarps) * kChunk + kWarps * 3 * kMaxN) * (int)sizeof(float);  // 81.5 KB
 
 // ---- launch 3: gradients of one chunk for a channel range. Warp w takes
 // channels d0 + w, d0 + w + 8, ...; per state n each warp rebuilds h over its
@@ -297,6 +300,7 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
     float *Bs = smem, *Cs = Bs + kMaxN * kChunk;
     float *accB = Cs + kMaxN * kChunk, *accC = accB + kMaxN * kChunk;  // [n][item][lane]
     float *redB = accC + kMaxN * kChunk, *redC = redB + kWarps * kChunk;  // [warp][item][lane]
+    float *spar = redC + kWarps * kChunk;  // [warp][A, entering state, leaving adjoint][n]
     const ChunkCtx c = chunk_ctx(p);
     load_bc_tiles(p, c, Bs, Cs, sizeof(IO) == 2);
     for (int i = threadIdx.x; i < kMaxN * kChunk; i += kThreads) accB[i] = accC[i] = 0.0f;
@@ -305,28 +309,40 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
     const int N = p.N;
     IO *dxp = static_cast<IO *>(p.dx);
     IO *ddp = static_cast<IO *>(p.ddelta);
+    float *par = spar + warp * 3 * kMaxN;
 
     for (int dbase = c.d0; dbase < c.d1; dbase += kWarps) {
         const int d = dbase + warp;
         const bool dok = d < c.d1;  // warp-uniform; absent channels add zeros
-        float dl[kItems], x[kItems], gy[kItems], v[kItems];
+        // this channel's A and carries for every n, read once
+        if (lane < N) {
+            const long long cidx = ((c.b * p.K + c.k) * p.D + d) * N + lane;
+            par[lane] = dok ? p.A[(long long)d * N + lane] : 0.0f;
+            par[kMaxN + lane] = dok ? p.carH[cidx] : 0.0f;
+            par[2 * kMaxN + lane] = dok ? p.carM[cidx] : 0.0f;
+        }
+        float dl[kItems], x[kItems], gy[kItems], v[kItems], xdl[kItems];
         load_items<IO>(p, c, d, dok, lane, dl, x, gy, v);
-        float gdl[kItems], gx[kItems];
+        // S = sum_n lam B (dx = dl S, ddelta gets x S), G = sum_n lam dA h_prev A
+        float S[kItems], G[kItems];
 #pragma unroll
-        for (int i = 0; i < kItems; ++i) gdl[i] = gx[i] = 0.0f;
+        for (int i = 0; i < kItems; ++i) {
+            xdl[i] = dl[i] * x[i];
+            S[i] = G[i] = 0.0f;
+        }
+        __syncwarp();
 
         for (int n = 0; n < N; ++n) {
-            const long long cidx = ((c.b * p.K + c.k) * p.D + d) * N + n;
-            const float An = dok ? p.A[(long long)d * N + n] : 0.0f;
-            const float A2 = An * kLog2e;
-            const float hs = dok ? p.carH[cidx] : 0.0f;  // state entering the chunk
-            const float me = dok ? p.carM[cidx] : 0.0f;  // adjoint leaving it
-            float dA[kItems], u[kItems], g[kItems], h[kItems];
+            const float An = par[n], A2 = An * kLog2e;
+            const float hs = par[kMaxN + n];      // state entering the chunk
+            const float me = par[2 * kMaxN + n];  // adjoint leaving it
+            float dA[kItems], u[kItems], g[kItems], Bv[kItems], h[kItems];
             Map f = {1.0f, 0.0f};
 #pragma unroll
             for (int i = 0; i < kItems; ++i) {
+                Bv[i] = Bs[n * kChunk + i * 32 + lane];
                 dA[i] = ex2_approx(dl[i] * A2);
-                u[i] = dl[i] * (x[i] * Bs[n * kChunk + i * 32 + lane]);
+                u[i] = xdl[i] * Bv[i];
                 g[i] = gy[i] * Cs[n * kChunk + i * 32 + lane];
                 f = {f.a * dA[i], fmaf(dA[i], f.b, u[i])};
             }
@@ -335,28 +351,25 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
             float hc = s;
 #pragma unroll
             for (int i = 0; i < kItems; ++i) h[i] = hc = fmaf(dA[i], hc, u[i]);
-            Map r = {1.0f, 0.0f};
+            float m = 0.0f;  // adjoint map of the lane's steps: mu -> f.a mu + m
 #pragma unroll
-            for (int i = kItems - 1; i >= 0; --i) r = {r.a * dA[i], dA[i] * (g[i] + r.b)};
-            const Map er = warp_exclusive_rev(r, lane);
+            for (int i = kItems - 1; i >= 0; --i) m = dA[i] * (g[i] + m);
+            const Map er = warp_exclusive_rev({f.a, m}, lane);
             float mu = fmaf(er.a, me, er.b);  // adjoint after this lane's last step
             float dAp = 0.0f;
 #pragma unroll
             for (int i = kItems - 1; i >= 0; --i) {
-                const float lam = g[i] + mu;                      // gradient of h_t
-                const float hprev = i > 0 ? h[i - 1] : s;
-                const float tA = lam * (dA[i] * hprev);           // through dA_t
-                const float Bv = Bs[n * kChunk + i * 32 + lane];
-                gdl[i] = fmaf(lam, Bv * x[i], gdl[i]);
-                gdl[i] = fmaf(tA, An, gdl[i]);
-                gx[i] = fmaf(lam, dl[i] * Bv, gx[i]);
+                const float lam = g[i] + mu;  // gradient of h_t
+                const float tA = lam * (dA[i] * (i > 0 ? h[i - 1] : s));  // through dA_t
+                S[i] = fmaf(lam, Bv[i], S[i]);
+                G[i] = fmaf(tA, An, G[i]);
                 dAp = fmaf(tA, dl[i], dAp);
-                redB[warp * kChunk + i * 32 + lane] = lam * (dl[i] * x[i]);
+                redB[warp * kChunk + i * 32 + lane] = lam * xdl[i];
                 redC[warp * kChunk + i * 32 + lane] = gy[i] * h[i];
                 mu = dA[i] * lam;
             }
             dAp = warp_sum(dAp);
-            if (dok && lane == 0) p.partA[cidx] = dAp;
+            if (dok && lane == 0) p.partA[((c.b * p.K + c.k) * p.D + d) * N + n] = dAp;
             __syncthreads();
             // this chunk's dB, dC for state n: the 8 warps' terms in warp order
             {
@@ -381,13 +394,15 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
                 sdx = fmaf(gy[i], x[i], sdx);
                 if (t < p.L) {
                     const long long gidx = (c.b * p.L + t) * p.D + d;
-                    st_io(dxp, gidx, fmaf(gy[i], Dd, gx[i]));
-                    st_io(ddp, gidx, p.softplus ? gdl[i] * softplus_grad(v[i]) : gdl[i]);
+                    const float gdl = fmaf(x[i], S[i], G[i]);
+                    st_io(dxp, gidx, fmaf(gy[i], Dd, dl[i] * S[i]));
+                    st_io(ddp, gidx, p.softplus ? gdl * softplus_grad(v[i]) : gdl);
                 }
             }
             sdx = warp_sum(sdx);
             if (lane == 0) p.partD[(c.b * p.K + c.k) * p.D + d] = sdx;
         }
+        __syncwarp();  // par is rewritten for the next channel
     }
     // this channel range's dB, dC over the chunk
     const int r = (int)(blockIdx.x % p.SD);
