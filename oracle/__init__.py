@@ -217,3 +217,27 @@ def s6_bwd(x, delta, Bt, Ct, A, Dskip, dy, h0=None, dh_last=None, softplus=False
     if rc:
         raise RuntimeError(f"oracle_s6_bwd_f64 failed ({rc})")
     return out
+
+
+# ---------------------------------------------------------------- layer
+def layer_fwd(x, W_proj, b_delta, A, Dskip, threads=1, lib: ctypes.CDLL | None = None):
+    """The selective-scan layer's forward pass ("POPCORNBENCH FW-GLM-5-1
+    l2_p30", the model's parameters and forward pass): the three input
+    projections, then the scan. W_proj is (D + 2N, D), PyTorch Linear layout:
+    rows [0, D) proj_delta, [D, D + N) proj_B, [D + N, D + 2N) proj_C.
+        delta = softplus(x W_delta^T + b_delta),  B_t = x W_B^T,  C_t = x W_C^T
+    The projections are float64 matrix products of the exact input values;
+    their results enter the float64 scan loop rounded once to float32 (the
+    loop's input type). Returns y (B, L, D) float64."""
+    x = _f32(x)
+    W = np.ascontiguousarray(W_proj, dtype=np.float32).astype(np.float64)
+    B, L, D = x.shape
+    N = (W.shape[0] - D) // 2
+    if W.shape != (D + 2 * N, D) or N < 1:
+        raise ValueError("W_proj must be (D + 2N, D)")
+    b = np.ascontiguousarray(b_delta, dtype=np.float32).astype(np.float64)
+    P = x.astype(np.float64).reshape(B * L, D) @ W.T                   # (B*L, D + 2N)
+    pre = (P[:, :D] + b).reshape(B, L, D).astype(np.float32)
+    Bt = P[:, D:D + N].reshape(B, L, N).astype(np.float32)
+    Ct = P[:, D + N:].reshape(B, L, N).astype(np.float32)
+    return s6_fwd(x, pre, Bt, Ct, A, Dskip, softplus=True, threads=threads, lib=lib)

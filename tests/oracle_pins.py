@@ -469,8 +469,40 @@ def pin_bwd_euler_and_skip(lib):
     assert chk(math.fsum((h0 * g0["dh0"]).ravel()), loss0, "h0"), "Euler identity in h0"
 
 
+# ---------------------------------------------------------------- layer pins
+def pin_layer_wiring(lib):
+    """Zero projections give y = D x; selector weights make B_t, C_t slices of
+    x and delta a constant, which must equal the scan run on those inputs
+    directly; a transposed or swapped weight block fails."""
+    g = _rng(40)
+    B, L, D, N = 2, 9, 6, 3
+    x = _dyadic(g, B * L * D, -2.0, 2.0, 6).reshape(B, L, D)
+    A = -g.uniform(0.2, 2.0, (D, N)).astype(np.float32)
+    Ds = g.standard_normal(D).astype(np.float32)
+    bd = g.uniform(-2.0, 1.0, D).astype(np.float32)
+    W = np.zeros((D + 2 * N, D), np.float32)
+    y = oracle.layer_fwd(x, W, bd, A, Ds, lib=lib)
+    assert np.array_equal(y, x.astype(np.float64) * Ds.astype(np.float64)), "zero projections"
+    # B_t = x[..., [1, 4, 2]], C_t = x[..., [5, 0, 3]], delta = softplus(bd)
+    for n, (cb, cc) in enumerate(((1, 5), (4, 0), (2, 3))):
+        W[D + n, cb] = 1.0
+        W[D + N + n, cc] = 1.0
+    y = oracle.layer_fwd(x, W, bd, A, Ds, lib=lib)
+    pre = np.broadcast_to(bd, (B, L, D)).copy()
+    ref = oracle.s6_fwd(x, pre, np.ascontiguousarray(x[..., [1, 4, 2]]),
+                        np.ascontiguousarray(x[..., [5, 0, 3]]), A, Ds, softplus=True, lib=lib)
+    assert np.array_equal(y, ref), "selector projections"
+    # proj_delta acts on x: W_delta = diag(1/4) gives delta = softplus(x/4 + bd)
+    W[:D, :D] = np.eye(D, dtype=np.float32) / 4
+    y = oracle.layer_fwd(x, W, bd, A, Ds, lib=lib)
+    pre = (x.astype(np.float64) / 4 + bd).astype(np.float32)
+    ref = oracle.s6_fwd(x, pre, np.ascontiguousarray(x[..., [1, 4, 2]]),
+                        np.ascontiguousarray(x[..., [5, 0, 3]]), A, Ds, softplus=True, lib=lib)
+    assert np.array_equal(y, ref), "delta projection and bias"
+
+
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_finite_differences_softplus,
-            pin_bwd_euler_and_skip]
+            pin_bwd_euler_and_skip, pin_layer_wiring]
 ALL_PINS = ALL_PINS + BWD_PINS
 
 
