@@ -220,7 +220,15 @@ def s6_bwd(x, delta, Bt, Ct, A, Dskip, dy, h0=None, dh_last=None, softplus=False
 
 
 # ---------------------------------------------------------------- layer
-def layer_fwd(x, W_proj, b_delta, A, Dskip, threads=1, lib: ctypes.CDLL | None = None):
+def _round_bf16(v):
+    """float64 values rounded once to bfloat16 (8 significant bits), to
+    nearest with ties to even; returned as float64."""
+    m, e = np.frexp(np.asarray(v, dtype=np.float64))  # v = m * 2**e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)
+
+
+def layer_fwd(x, W_proj, b_delta, A, Dskip, io="f32", threads=1,
+              lib: ctypes.CDLL | None = None):
     """The selective-scan layer's forward pass ("POPCORNBENCH FW-GLM-5-1
     l2_p30", the model's parameters and forward pass): the three input
     projections, then the scan. W_proj is (D + 2N, D), PyTorch Linear layout:
@@ -228,7 +236,9 @@ def layer_fwd(x, W_proj, b_delta, A, Dskip, threads=1, lib: ctypes.CDLL | None =
         delta = softplus(x W_delta^T + b_delta),  B_t = x W_B^T,  C_t = x W_C^T
     The projections are float64 matrix products of the exact input values;
     their results enter the float64 scan loop rounded once to float32 (the
-    loop's input type). Returns y (B, L, D) float64."""
+    loop's input type). With io == "bf16" the projections are first rounded
+    once to bfloat16, as a Linear layer in that storage type returns them;
+    the delta bias is added after that rounding. Returns y (B, L, D) float64."""
     x = _f32(x)
     W = np.ascontiguousarray(W_proj, dtype=np.float32).astype(np.float64)
     B, L, D = x.shape
@@ -237,6 +247,8 @@ def layer_fwd(x, W_proj, b_delta, A, Dskip, threads=1, lib: ctypes.CDLL | None =
         raise ValueError("W_proj must be (D + 2N, D)")
     b = np.ascontiguousarray(b_delta, dtype=np.float32).astype(np.float64)
     P = x.astype(np.float64).reshape(B * L, D) @ W.T                   # (B*L, D + 2N)
+    if io == "bf16":
+        P = _round_bf16(P)
     pre = (P[:, :D] + b).reshape(B, L, D).astype(np.float32)
     Bt = P[:, D:D + N].reshape(B, L, N).astype(np.float32)
     Ct = P[:, D + N:].reshape(B, L, N).astype(np.float32)

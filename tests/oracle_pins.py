@@ -501,8 +501,22 @@ def pin_layer_wiring(lib):
     assert np.array_equal(y, ref), "delta projection and bias"
 
 
+def pin_bf16_rounding(lib):
+    """The bfloat16 rounding the layer oracle applies: values with at most 8
+    significant bits are unchanged; halfway cases go to the even neighbour;
+    otherwise the nearer neighbour."""
+    r = oracle._round_bf16
+    exact = np.array([1.0, -3.0, 0.75, 255.0, 2.0 ** -20 * 129, 1.5e-3 * 0 + 0.5])
+    assert np.array_equal(r(exact), exact)
+    # 1 + 2**-8 lies halfway between 1 and 1 + 2**-7: ties to even gives 1
+    assert r(np.array([1.0 + 2.0 ** -8]))[0] == 1.0
+    assert r(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 1.0 + 2 * 2.0 ** -7  # tie, to even
+    assert r(np.array([1.0 + 2.0 ** -8 + 2.0 ** -30]))[0] == 1.0 + 2.0 ** -7
+    assert r(np.array([-(1.0 + 2.0 ** -8 + 2.0 ** -30)]))[0] == -(1.0 + 2.0 ** -7)
+
+
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_finite_differences_softplus,
-            pin_bwd_euler_and_skip, pin_layer_wiring]
+            pin_bwd_euler_and_skip, pin_layer_wiring, pin_bf16_rounding]
 ALL_PINS = ALL_PINS + BWD_PINS
 
 
