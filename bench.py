@@ -229,7 +229,7 @@ def s6_variant(name):
     """(workload, variant) for an S6 bench name: "s6_x", "s6_x_state" or
     "s6_x_bwd"."""
     import workloads
-    for suffix in ("_state", "_bwd"):
+    for suffix in ("_state", "_bwd", "_layer"):
         if name.endswith(suffix) and name[: -len(suffix)] in workloads.S6:
             return workloads.S6[name[: -len(suffix)]], suffix[1:]
     return workloads.S6[name], ""
@@ -266,6 +266,27 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
         call = lambda: ss.ss_selective_scan_fwd_state(*args, h0=h0, delta_softplus=w.softplus,
                                                       y=y, h_last=h_last, stream=stream)
         byts += 2 * 4 * w.B * w.D * w.N
+    t_gemm = 0.0
+    if variant == "layer":
+        # projections of the workload's shape with seeded random weights:
+        # W ~ N(0, 1/D), b_delta ~ N(-4, 1) (steps like the workload's)
+        g = np.random.Generator(np.random.PCG64(23))
+        W = t(g.standard_normal((w.D + 2 * w.N, w.D)).astype(np.float32) / np.sqrt(w.D))
+        if inp.io == "bf16":
+            W = W.to(torch.bfloat16)
+        bd = torch.from_numpy(g.normal(-4.0, 1.0, w.D).astype(np.float32)).to(dev)
+        io_dtype = ss.SS_BF16 if w.io == "bf16" else ss.SS_F32
+        lws = ss.new_workspace(
+            ss.ss_selective_scan_layer_workspace_bytes(w.B, w.L, w.D, w.N, io_dtype), dev)
+        call = lambda: ss.ss_selective_scan_layer_fwd(args[0], W, bd, args[4], args[5], y=y,
+                                                      workspace=lws, stream=stream)
+        es = 2 if w.io == "bf16" else 4
+        M = w.B * w.L
+        gemm_flops = 2.0 * M * w.D * (w.D + 2 * w.N)
+        peaks, _ = measured_peaks()
+        t_gemm = gemm_flops / (float(peaks.get("bf16_tflops", 1900.0)) * 1e12)
+        # x and W read, projections written and read back by the scan
+        byts += es * (w.D + 2 * w.N) * w.D + 2 * es * M * (w.D + 2 * w.N)
     if variant == "bwd":
         g = np.random.Generator(np.random.PCG64(17))
         dy = t(g.standard_normal((w.B, w.L, w.D)).astype(np.float32))
@@ -286,7 +307,7 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
     ms = statistics.mean(per)
     t_hbm = byts / (hbm_peak * 1e9)
     t_sfu = mufu / sfu_peak
-    t_roof = max(t_hbm, t_sfu)
+    t_roof = max(t_hbm, t_sfu) + t_gemm
     return {
         "elements": w.elements, "shape": [w.B, w.L, w.D, w.N], "io": w.io,
         "softplus": w.softplus, "bidir": w.bidir, "variant": variant or "forward", "ms": ms,
@@ -294,11 +315,15 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
         "elements_per_s": w.elements / (ms * 1e-3),
         "gbs": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts, "mufu_ops": mufu,
         "t_hbm_us": t_hbm * 1e6, "t_sfu_us": t_sfu * 1e6,
+        **({"t_gemm_us": t_gemm * 1e6, "gemm_peak": "measured bf16_tflops"} if t_gemm else {}),
         "bound": "hbm" if t_hbm >= t_sfu else "sfu",
         "roofline_frac": t_roof / (ms * 1e-3),
         "l2": "flushed between calls" if flush else "inputs larger than L2",
         "workspace_bytes": (
             ss.ss_selective_scan_bwd_workspace_bytes(w.B, w.L, w.D, w.N) if variant == "bwd" else
+            ss.ss_selective_scan_layer_workspace_bytes(
+                w.B, w.L, w.D, w.N, ss.SS_BF16 if w.io == "bf16" else ss.SS_F32)
+            if variant == "layer" else
             ss.ss_selective_scan_workspace_bytes(w.B, w.L, w.D, w.N,
                                                  ss.SS_BF16 if w.io == "bf16" else ss.SS_F32,
                                                  w.bidir)),
@@ -435,7 +460,7 @@ def run_ours(args, rank, world, local_rank):
                              "elements_per_s": w.n / (launch_ms * 1e-3), "gbs": achieved,
                              "bound": "hbm", "roofline_frac": achieved / hbm_peak}
         for name in ("s6_fp32", "s6_bf16", "s6_bidir", "s6_bf16_state", "s6_fp32_bwd",
-                     "s6_bf16_bwd"):
+                     "s6_bf16_bwd", "s6_bf16_layer"):
             per_cfg[name] = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream,
                                      hbm_peak, sfu)
         extras["per_config"] = per_cfg
@@ -480,7 +505,7 @@ def run_single(args):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     name = args.workload
     if name in workloads.S6 or any(name.endswith(x) and name[: -len(x)] in workloads.S6
-                                   for x in ("_state", "_bwd")):
+                                   for x in ("_state", "_bwd", "_layer")):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         sfu = mufu_probe(torch, ss, dev, sms) if not args.no_extras else 9.86e12
         r = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream, hbm_peak, sfu)
@@ -513,7 +538,8 @@ def main():
                     help="with --workload affine_*: use this many elements (small ncu captures)")
     ap.add_argument("--workload", default=HEADLINE,
                     help="time one workload only (affine_small, affine_large, s6_fp32, "
-                         "s6_bf16, s6_bidir, s6_bf16_state, s6_fp32_bwd, s6_bf16_bwd); the default "
+                         "s6_bf16, s6_bidir, s6_bf16_state, s6_fp32_bwd, s6_bf16_bwd, s6_bf16_layer); "
+                         "the default "
                          "is the full benchmark")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -197,6 +197,37 @@ ss_status ss_selective_scan_fwd_state(const void *x, const void *delta,
                                       void *stream);
 
 /*
+ * Selective-scan layer forward ("POPCORNBENCH FW-GLM-5-1 l2_p30", the
+ * model's parameters and forward pass): the input projections, then the
+ * scan of ss_selective_scan_fwd:
+ *   delta = softplus(x W_delta^T + b_delta)   (B, L, D)
+ *   B_t = x W_B^T,  C_t = x W_C^T             (B, L, N)
+ *   y = S6(x, delta, B_t, C_t, A, Dskip)      (B, L, D)
+ * x, y: (B, L, D) of io_dtype. W_proj: (D + 2N, D) of io_dtype, row-major in
+ * the Linear weight layout (out_features x in_features): rows [0, D) are
+ * proj_delta, [D, D + N) proj_B, [D + N, D + 2N) proj_C. b_delta: (D,) fp32.
+ * A: (D, N) fp32 (already negative); Dskip: (D,) fp32 or NULL. proj_B and
+ * proj_C carry no bias (the pages give one for proj_delta only).
+ * The projections are dense GEMMs run by cuBLASLt with fp32 accumulation
+ * into the workspace (projection outputs in io_dtype); the bias and softplus
+ * are applied inside the scan. The workspace
+ * (ss_selective_scan_layer_workspace_bytes) holds the projections, the
+ * GEMM scratch and the scan's workspace (first, so ss_get_device_status
+ * reads the scan's error word from it); zero it once before first use, as
+ * for the scan. Errors as for ss_selective_scan_fwd; SS_ERR_UNSUPPORTED if
+ * no GEMM algorithm fits the shape.
+ */
+size_t ss_selective_scan_layer_workspace_bytes(int64_t B, int64_t L, int64_t D,
+                                               int64_t N, int io_dtype);
+
+ss_status ss_selective_scan_layer_fwd(const void *x, const void *W_proj,
+                                      const float *b_delta, const float *A,
+                                      const float *Dskip, void *y,
+                                      int64_t B, int64_t L, int64_t D, int64_t N,
+                                      int io_dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/*
  * Backward pass of ss_selective_scan_fwd_state: the gradients of the scalar
  * sum_{b,t,d} dy*y + sum_{b,d,n} dh_last*h_last with respect to every input,
  * i.e. the exact derivative of the forward recurrence ("POPCORNBENCH

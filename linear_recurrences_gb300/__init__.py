@@ -28,6 +28,7 @@ __all__ = [
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
     "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
+    "ss_selective_scan_layer_fwd", "ss_selective_scan_layer_workspace_bytes",
     "new_workspace", "EXPORTED_SYMBOLS",
 ]
 
@@ -41,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_selective_scan_fwd_state",
     "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
+    "ss_selective_scan_layer_workspace_bytes", "ss_selective_scan_layer_fwd",
 )
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -107,6 +109,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_selective_scan_bwd_workspace_bytes.restype = sz
     L.ss_selective_scan_bwd.argtypes = [vp] * 16 + [i64, i64, i64, i64, ci, ci, vp, sz, vp]
     L.ss_selective_scan_bwd.restype = ci
+    L.ss_selective_scan_layer_workspace_bytes.argtypes = [i64, i64, i64, i64, ci]
+    L.ss_selective_scan_layer_workspace_bytes.restype = sz
+    L.ss_selective_scan_layer_fwd.argtypes = [vp] * 6 + [i64, i64, i64, i64, ci, vp, sz, vp]
+    L.ss_selective_scan_layer_fwd.restype = ci
     return L
 
 
@@ -374,3 +380,43 @@ def ss_selective_scan_bwd(x, delta, Bt, Ct, A, Dskip, dy, h0=None, dh_last=None,
     if st != SS_OK:
         raise SSError(st, "ss_selective_scan_bwd")
     return out
+
+
+def ss_selective_scan_layer_workspace_bytes(B, L, D, N, io_dtype=SS_F32) -> int:
+    return lib().ss_selective_scan_layer_workspace_bytes(int(B), int(L), int(D), int(N),
+                                                         int(io_dtype))
+
+
+def ss_selective_scan_layer_fwd(x, W_proj, b_delta, A, Dskip=None, y=None, workspace=None,
+                                stream=None):
+    """Selective-scan layer forward: delta = softplus(x W_delta^T + b_delta),
+    B_t = x W_B^T, C_t = x W_C^T (W_proj (D + 2N, D), rows proj_delta |
+    proj_B | proj_C), then the scan; returns y (B, L, D) in x's dtype."""
+    torch = _torch()
+    _check_cuda(x, "x", (torch.float32, torch.bfloat16))
+    _check_cuda(W_proj, "W_proj", (x.dtype,))
+    _check_cuda(b_delta, "b_delta", (torch.float32,))
+    _check_cuda(A, "A", (torch.float32,))
+    if Dskip is not None:
+        _check_cuda(Dskip, "Dskip", (torch.float32,))
+    B, L, D = x.shape
+    N = A.shape[1]
+    if W_proj.shape != (D + 2 * N, D) or A.shape != (D, N) or b_delta.shape != (D,):
+        raise ValueError("W_proj must be (D + 2N, D), A (D, N), b_delta (D,)")
+    if y is None:
+        y = torch.empty_like(x)
+    _check_cuda(y, "y", (x.dtype,))
+    io_dtype = SS_BF16 if x.dtype == torch.bfloat16 else SS_F32
+    sh = _stream_handle(stream, x.device)
+    need = ss_selective_scan_layer_workspace_bytes(B, L, D, N, io_dtype)
+    if workspace is None and need:
+        key = ("ss_selective_scan_layer_fwd", B, L, D, N, io_dtype, need,
+               os.environ.get("SS_S6_WT_TSUB"))
+        workspace = _cached_workspace(key, need, x.device, sh)
+    wsb = workspace.numel() if workspace is not None else 0
+    st = lib().ss_selective_scan_layer_fwd(_ptr(x), _ptr(W_proj), _ptr(b_delta), _ptr(A),
+                                           _ptr(Dskip), _ptr(y), B, L, D, N, io_dtype,
+                                           _ptr(workspace), wsb, sh)
+    if st != SS_OK:
+        raise SSError(st, "ss_selective_scan_layer_fwd")
+    return y

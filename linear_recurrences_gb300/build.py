@@ -75,7 +75,11 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
+    # cuBLASLt (the projection GEMMs of the layer entry point) is linked
+    # dynamically from the toolkit next to nvcc
+    cudalib = os.path.realpath(os.path.join(os.path.dirname(cc), "..", "lib64"))
+    cmd = [cc, *ARCH, "-shared", "-cudart", "static", *objs, "-L", cudalib, "-lcublasLt",
+           "-Xlinker", "-rpath", "-Xlinker", cudalib, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

@@ -1,0 +1,147 @@
+// Selective-scan layer forward: the three input projections, then the scan.
+//
+// "POPCORNBENCH FW-GLM-5-1 l2_p30", the model's parameters and forward pass:
+// delta = softplus(proj_delta(x)) with a bias, B_t = proj_B(x), C_t =
+// proj_C(x), then the S6 recurrence. The projections are plain dense GEMMs
+// (x is (B*L) x D, the weights D x D and D x N) and run as cuBLASLt matmuls
+// (bf16 or fp32 inputs, fp32 accumulation) into the workspace; the delta
+// bias and softplus are fused into the scan, which reads the projections
+// straight from there.
+#include <cublasLt.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "ss_common.cuh"
+#include "ss_internal.h"
+
+namespace ss {
+namespace {
+
+constexpr size_t kLtWorkspace = 32u << 20;  // cuBLASLt scratch per call
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+cublasLtHandle_t lt_handle() {
+    static std::once_flag once;
+    static cublasLtHandle_t h = nullptr;
+    std::call_once(once, [] {
+        if (cublasLtCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
+    });
+    return h;
+}
+
+// out (M x nout, row-major) = x (M x K, row-major) * W^T, W (nout x K,
+// row-major: the Linear weight layout). In cuBLAS's column-major terms:
+// out^T (nout x M) = op(W) * x^T with W viewed as K x nout, transposed.
+ss_status gemm_xwT(const void *x, const void *W, void *out, int64_t M, int64_t K, int64_t nout,
+                   bool bf16, void *lt_ws, cudaStream_t stream) {
+    cublasLtHandle_t h = lt_handle();
+    if (!h) return SS_ERR_CUDA;
+    const cudaDataType_t t = bf16 ? CUDA_R_16BF : CUDA_R_32F;
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+    cublasLtMatmulPreference_t pref = nullptr;
+    ss_status st = SS_ERR_CUDA;
+    const cublasOperation_t ta = CUBLAS_OP_T, tb = CUBLAS_OP_N;
+    const size_t wsb = kLtWorkspace;
+    cublasLtMatmulHeuristicResult_t heur{};
+    int found = 0;
+    const float alpha = 1.0f, beta = 0.0f;
+    if (cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &ta, sizeof(ta)) !=
+            CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &tb, sizeof(tb)) !=
+            CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&la, t, (uint64_t)K, (uint64_t)nout, K) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&lb, t, (uint64_t)K, (uint64_t)M, K) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatrixLayoutCreate(&lc, t, (uint64_t)nout, (uint64_t)M, nout) !=
+            CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulPreferenceCreate(&pref) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb,
+                                             sizeof(wsb)) != CUBLAS_STATUS_SUCCESS ||
+        cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, lc, lc, pref, 1, &heur, &found) !=
+            CUBLAS_STATUS_SUCCESS ||
+        found < 1) {
+        st = SS_ERR_UNSUPPORTED;
+    } else if (cublasLtMatmul(h, op, &alpha, W, la, x, lb, &beta, out, lc, out, lc, &heur.algo,
+                              lt_ws, wsb, stream) == CUBLAS_STATUS_SUCCESS) {
+        st = SS_OK;
+    }
+    if (pref) cublasLtMatmulPreferenceDestroy(pref);
+    if (lc) cublasLtMatrixLayoutDestroy(lc);
+    if (lb) cublasLtMatrixLayoutDestroy(lb);
+    if (la) cublasLtMatrixLayoutDestroy(la);
+    if (op) cublasLtMatmulDescDestroy(op);
+    return st;
+}
+
+struct LayerPlan {
+    size_t pre, bt, ct, lt, scan, total;  // section offsets, then total bytes
+};
+
+LayerPlan layer_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16) {
+    LayerPlan pl{};
+    const size_t es = io_bf16 ? 2 : 4;
+    const size_t M = (size_t)(B * L);
+    // the scan's section comes first, so the workspace starts with its
+    // header (error word) even when the scan needs no further workspace
+    pl.scan = 0;
+    pl.pre = std::max<size_t>(kWsHeaderBytes, align256(s6_workspace_bytes(B, L, D, N, io_bf16, 0)));
+    pl.bt = pl.pre + align256(M * D * es);
+    pl.ct = pl.bt + align256(M * N * es);
+    pl.lt = pl.ct + align256(M * N * es);
+    pl.total = pl.lt + kLtWorkspace;
+    return pl;
+}
+
+}  // namespace
+
+size_t layer_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16) {
+    if (B <= 0 || L <= 0 || D <= 0 || N <= 0) return 0;
+    return layer_plan(B, L, D, N, io_bf16).total;
+}
+
+ss_status layer_fwd_launch(const void *x, const void *W_proj, const float *b_delta, const float *A,
+                           const float *Dskip, void *y, int64_t B, int64_t L, int64_t D,
+                           int64_t N, int io_bf16, void *workspace, size_t ws_bytes,
+                           cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit) {
+    const LayerPlan pl = layer_plan(B, L, D, N, io_bf16);
+    if (workspace == nullptr || ws_bytes < pl.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return SS_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(workspace);
+    const size_t es = io_bf16 ? 2 : 4;
+    const char *Wc = static_cast<const char *>(W_proj);
+    const int64_t M = B * L;
+    // rows [0, D) of W_proj: proj_delta; [D, D + N): proj_B; [D + N, D + 2N): proj_C
+    ss_status st = gemm_xwT(x, Wc, ws + pl.pre, M, D, D, io_bf16, ws + pl.lt, stream);
+    if (st == SS_OK)
+        st = gemm_xwT(x, Wc + (size_t)D * D * es, ws + pl.bt, M, D, N, io_bf16, ws + pl.lt, stream);
+    if (st == SS_OK)
+        st = gemm_xwT(x, Wc + (size_t)(D + N) * D * es, ws + pl.ct, M, D, N, io_bf16, ws + pl.lt,
+                      stream);
+    if (st != SS_OK) return st;
+    S6Args a;
+    a.x = x;
+    a.delta = ws + pl.pre;
+    a.Bt = ws + pl.bt;
+    a.Ct = ws + pl.ct;
+    a.A = A;
+    a.Dskip = Dskip;
+    a.y = y;
+    a.delta_bias = b_delta;
+    a.h0 = nullptr;
+    a.h_last = nullptr;
+    a.B = B;
+    a.L = L;
+    a.D = D;
+    a.N = N;
+    a.io_bf16 = io_bf16;
+    a.softplus = 1;
+    a.bidir = 0;
+    return s6_launch(a, ws + pl.scan, pl.pre - pl.scan, stream, timeout_ns, skip_unit);
+}
+
+}  // namespace ss

@@ -80,6 +80,7 @@ struct S6Params {
     float *payload;    // [((seq*K + k)*NF + field)*32*NG + lane*NG + i]
     unsigned long long timeout_ns;
     long long skip_unit;  // test hook: this unit publishes nothing (-1: none)
+    const float *delta_bias;  // (D,) added to delta before softplus, or null
     const float *h0;      // (B, D, N) state before t = 0, or null (zeros); forward only
     float *h_last;        // (B, D, N) receives the state after t = L - 1, or null
 };
@@ -187,6 +188,7 @@ struct WarpCtx {
     int ch;                // channel of this lane within the warp's tile
     int half;              // which NG-state slice of the channel this lane holds
     bool dvalid;
+    float dbias;           // bias added to this channel's delta (0 if none)
     long long t0, t1;      // this warp's timesteps
 };
 
@@ -441,7 +443,7 @@ __device__ __forceinline__ void sweep(const S6Params &p, WarpCtx &w, const u64 (
                 for (int rr = 0; rr < 8; ++rr) {
                     const int r = REV ? kTS - 1 - (r0 + rr) : r0 + rr;
                     step<NG, LPC, IO, SP, BIDIR, MODE, OUT>(
-                        to_f32(xs[r * CPW]), to_f32(ds[r * CPW]), bf + r * bstride,
+                        to_f32(xs[r * CPW]), to_f32(ds[r * CPW]) + w.dbias, bf + r * bstride,
                         cf + r * bstride, A2, Dd, h, hr, Q, sdel, yp + r * D,
                         yfp ? yfp + r * D : nullptr, yfv[rr], store);
                 }
@@ -450,7 +452,7 @@ __device__ __forceinline__ void sweep(const S6Params &p, WarpCtx &w, const u64 (
             for (int rr = 0; rr < nrows; ++rr) {
                 const int r = REV ? nrows - 1 - rr : rr;
                 const float yfv = (OUT == OUT_SUM && store) ? __ldcg(yfp + r * D) : 0.0f;
-                step<NG, LPC, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * CPW]), to_f32(ds[r * CPW]),
+                step<NG, LPC, IO, SP, BIDIR, MODE, OUT>(to_f32(xs[r * CPW]), to_f32(ds[r * CPW]) + w.dbias,
                                                         bf + r * bstride, cf + r * bstride, A2, Dd,
                                                         h, hr, Q, sdel, yp + r * D,
                                                         yfp ? yfp + r * D : nullptr, yfv, store);
@@ -631,6 +633,7 @@ s6_kernel(const __grid_constant__ S6Params p) {
         A2[q] = f2(lo, hi);
     }
     const float Dd = (w.dvalid && p.Dskip) ? p.Dskip[w.d] : 0.0f;
+    w.dbias = (w.dvalid && p.delta_bias) ? p.delta_bias[w.d] : 0.0f;
 
     u64 h[NP], hr[NP], Q[NP];
     float sdel = 0.0f;
@@ -996,6 +999,7 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
     }
     prm.timeout_ns = timeout_ns;
     prm.skip_unit = skip_unit;
+    prm.delta_bias = a.delta_bias;
     prm.h0 = a.bidir ? nullptr : a.h0;
     prm.h_last = a.bidir ? nullptr : a.h_last;
     char *ws = static_cast<char *>(workspace);

@@ -123,6 +123,33 @@ ss_status ss_selective_scan_fwd_state(const void *x, const void *delta, const vo
                     workspace_bytes, stream, 0, h0, h_last);
 }
 
+size_t ss_selective_scan_layer_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N,
+                                               int io_dtype) {
+    if (N < 1 || N > 16 || (io_dtype != SS_F32 && io_dtype != SS_BF16)) return 0;
+    return ss::layer_workspace_bytes(B, L, D, N, io_dtype == SS_BF16);
+}
+
+ss_status ss_selective_scan_layer_fwd(const void *x, const void *W_proj, const float *b_delta,
+                                      const float *A, const float *Dskip, void *y, int64_t B,
+                                      int64_t L, int64_t D, int64_t N, int io_dtype,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+    if (B < 0 || L < 0 || D < 0 || N < 0) return SS_ERR_INVALID;
+    if (io_dtype != SS_F32 && io_dtype != SS_BF16) return SS_ERR_INVALID;
+    if (N < 1 || N > 16) return SS_ERR_UNSUPPORTED;
+    if (B == 0 || L == 0 || D == 0) return SS_OK;
+    if (!x || !W_proj || !b_delta || !A || !y) return SS_ERR_INVALID;
+    const uintptr_t es = io_dtype == SS_BF16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(W_proj, es) || !aligned(y, es) || !aligned(b_delta, 4) ||
+        !aligned(A, 4) || !aligned(Dskip, 4))
+        return SS_ERR_INVALID;
+    if (B > (1LL << 31) || L > (1LL << 40) || D > (1LL << 31) || B * L > (1LL << 48))
+        return SS_ERR_UNSUPPORTED;
+    return ss::layer_fwd_launch(x, W_proj, b_delta, A, Dskip, y, B, L, D, N,
+                                io_dtype == SS_BF16, workspace, workspace_bytes,
+                                static_cast<cudaStream_t>(stream), g_timeout_ns.load(),
+                                take_skip_unit());
+}
+
 size_t ss_selective_scan_bwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
     if (N < 1 || N > 16) return 0;
     return ss::s6_bwd_workspace_bytes(B, L, D, N);

@@ -17,6 +17,7 @@ struct S6Args {
     const void *x, *delta, *Bt, *Ct;
     const float *A, *Dskip;
     void *y;
+    const float *delta_bias = nullptr;  // (D,) added to delta before softplus, or null
     const float *h0;  // (B, D, N) initial state or null (zeros); forward only
     float *h_last;    // (B, D, N) final state or null; forward only
     int64_t B, L, D, N;
@@ -40,6 +41,11 @@ struct S6BwdArgs {
     int softplus;
 };
 size_t s6_bwd_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N);
+size_t layer_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16);
+ss_status layer_fwd_launch(const void *x, const void *W_proj, const float *b_delta, const float *A,
+                           const float *Dskip, void *y, int64_t B, int64_t L, int64_t D,
+                           int64_t N, int io_bf16, void *workspace, size_t ws_bytes,
+                           cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit);
 ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cudaStream_t stream);
 ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStream_t stream,
                     unsigned long long timeout_ns, long long skip_unit);
