@@ -459,6 +459,17 @@ def run_ours(args, rank, world, local_rank):
         per_cfg[HEADLINE] = {"elements": w.n, "ms": launch_ms,
                              "elements_per_s": w.n / (launch_ms * 1e-3), "gbs": achieved,
                              "bound": "hbm", "roofline_frac": achieved / hbm_peak}
+        # comparison kernel: the same scan with log-step (Hillis-Steele) tiles
+        lws = ss.new_workspace(ss.ss_affine_scan_workspace_bytes(w.n), dev)
+        lper, _ = time_launches(
+            torch, lambda: ss.ss_affine_scan_log_step(a, b, h, workspace=lws, stream=stream),
+            args.steps, args.warmup, stream)
+        lms = statistics.mean(lper)
+        per_cfg[HEADLINE + "_log_step"] = {
+            "elements": w.n, "ms": lms, "elements_per_s": w.n / (lms * 1e-3),
+            "gbs": 12 * w.n / (lms * 1e-3) / 1e9, "roofline_frac": 12 * w.n / (lms * 1e-3) / 1e9 / hbm_peak,
+            "kernel": "comparison: log-step (Hillis-Steele) tile scan, same look-back"}
+        del lws
         for name in ("s6_fp32", "s6_bf16", "s6_bidir", "s6_bf16_state", "s6_fp32_bwd",
                      "s6_bf16_bwd", "s6_bf16_layer"):
             per_cfg[name] = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream,
@@ -509,21 +520,24 @@ def run_single(args):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         sfu = mufu_probe(torch, ss, dev, sms) if not args.no_extras else 9.86e12
         r = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream, hbm_peak, sfu)
-    elif name in workloads.AFFINE:
+    elif name in workloads.AFFINE or (name.endswith("_log_step") and name[:-9] in workloads.AFFINE):
+        log_step = name.endswith("_log_step")
+        name = name[:-9] if log_step else name
+        fn = ss.ss_affine_scan_log_step if log_step else ss.ss_affine_scan
         w, _, _, a, b = affine_setup(torch, dev, name)
         if args.affine_n:
             w = workloads.AffineWorkload(name, args.affine_n, w.a_lo, w.a_hi)
             a, b = a[: w.n].contiguous(), b[: w.n].contiguous()
         h = torch.empty_like(a)
         ws = ss.new_workspace(ss.ss_affine_scan_workspace_bytes(w.n), dev)
-        per, _ = time_launches(torch, lambda: ss.ss_affine_scan(a, b, h, workspace=ws, stream=stream),
+        per, _ = time_launches(torch, lambda: fn(a, b, h, workspace=ws, stream=stream),
                                args.steps, args.warmup, stream)
         ms = statistics.mean(per)
         r = {"elements": w.n, "ms": ms, "elements_per_s": w.n / (ms * 1e-3),
              "gbs": 12 * w.n / (ms * 1e-3) / 1e9, "roofline_frac": 12 * w.n / (ms * 1e-3) / 1e9 / hbm_peak}
     else:
         raise SystemExit(f"unknown workload {name}")
-    print(json.dumps({"workload": name, "steps": args.steps, "warmup": args.warmup, **r}), flush=True)
+    print(json.dumps({"workload": args.workload, "steps": args.steps, "warmup": args.warmup, **r}), flush=True)
 
 
 def main():
@@ -538,7 +552,8 @@ def main():
                     help="with --workload affine_*: use this many elements (small ncu captures)")
     ap.add_argument("--workload", default=HEADLINE,
                     help="time one workload only (affine_small, affine_large, s6_fp32, "
-                         "s6_bf16, s6_bidir, s6_bf16_state, s6_fp32_bwd, s6_bf16_bwd, s6_bf16_layer); "
+                         "affine_large_log_step, s6_bf16, s6_bidir, s6_bf16_state, s6_fp32_bwd, s6_bf16_bwd, "
+                         "s6_bf16_layer); "
                          "the default "
                          "is the full benchmark")
     args = ap.parse_args()

@@ -98,6 +98,23 @@ ss_status ss_affine_scan(const float *a, const float *b, float *h, int64_t n,
                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Comparison kernel, not the fast path: ss_affine_scan with each tile scanned
+ * by the log-step (Hillis-Steele) algorithm instead of the work-efficient
+ * register scan, inside the same persistent look-back kernel. "Selective-scan
+ * CUDA kernels" (persus.netlify.app), the predictions: the page's
+ * Hillis-Steele measurement ran in PyTorch, which the page itself calls an
+ * unfair comparison with its single-pass kernel; this one runs on the GPU
+ * under identical staging, look-back and fix-up, so the two measure the
+ * algorithms. Each 4096-element tile takes 12 steps; in step k every element
+ * E >= 2^k is combined with element E - 2^k as it was after step k-1 (values
+ * in registers, exchanged through the tile's shared-memory buffer). Same
+ * arguments, workspace (ss_affine_scan_workspace_bytes), results up to
+ * rounding order (deterministic) and errors as ss_affine_scan.
+ */
+ss_status ss_affine_scan_log_step(const float *a, const float *b, float *h, int64_t n,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Largest n ss_affine_scan_noalloc accepts (2^24 elements). Its scratch
  * array is 256 + 32 * (SS_AFFINE_NOALLOC_MAX_N / 4096) = 131,328 bytes.
  */

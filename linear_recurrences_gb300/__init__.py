@@ -29,7 +29,7 @@ __all__ = [
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
     "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
     "ss_selective_scan_layer_fwd", "ss_selective_scan_layer_workspace_bytes",
-    "new_workspace", "EXPORTED_SYMBOLS",
+    "ss_affine_scan_log_step", "new_workspace", "EXPORTED_SYMBOLS",
 ]
 
 SS_OK, SS_ERR_INVALID, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -43,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_selective_scan_fwd_state",
     "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
     "ss_selective_scan_layer_workspace_bytes", "ss_selective_scan_layer_fwd",
+    "ss_affine_scan_log_step",
 )
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -113,6 +114,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_selective_scan_layer_workspace_bytes.restype = sz
     L.ss_selective_scan_layer_fwd.argtypes = [vp] * 6 + [i64, i64, i64, i64, ci, vp, sz, vp]
     L.ss_selective_scan_layer_fwd.restype = ci
+    L.ss_affine_scan_log_step.argtypes = [vp, vp, vp, i64, vp, sz, vp]
+    L.ss_affine_scan_log_step.restype = ci
     return L
 
 
@@ -200,7 +203,7 @@ def ss_affine_scan_workspace_bytes(n: int) -> int:
     return lib().ss_affine_scan_workspace_bytes(int(n))
 
 
-def ss_affine_scan(a, b, h=None, workspace=None, stream=None):
+def ss_affine_scan(a, b, h=None, workspace=None, stream=None, _fn="ss_affine_scan"):
     """h[t] = a[t]*h[t-1] + b[t] (fp32, 1-D, on the GPU). Returns h."""
     torch = _torch()
     _check_cuda(a, "a", (torch.float32,))
@@ -218,10 +221,16 @@ def ss_affine_scan(a, b, h=None, workspace=None, stream=None):
     if workspace is None and need:
         workspace = _cached_workspace(("affine",), need, a.device, sh)
     wsb = workspace.numel() if workspace is not None else 0
-    st = lib().ss_affine_scan(_ptr(a), _ptr(b), _ptr(h), n, _ptr(workspace), wsb, sh)
+    st = getattr(lib(), _fn)(_ptr(a), _ptr(b), _ptr(h), n, _ptr(workspace), wsb, sh)
     if st != SS_OK:
-        raise SSError(st, "ss_affine_scan")
+        raise SSError(st, _fn)
     return h
+
+
+def ss_affine_scan_log_step(a, b, h=None, workspace=None, stream=None):
+    """The affine scan with a log-step (Hillis-Steele) scan of each tile: a
+    comparison kernel for the work-efficient ss_affine_scan."""
+    return ss_affine_scan(a, b, h, workspace, stream, _fn="ss_affine_scan_log_step")
 
 
 SS_AFFINE_NOALLOC_MAX_N = 1 << 24

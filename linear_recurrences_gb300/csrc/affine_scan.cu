@@ -214,6 +214,100 @@ __device__ __forceinline__ void scan_tile(const AffineParams &p, unsigned tile, 
     compute_sync();  // s_warp is free for the next tile
 }
 
+// ---- comparison variant: a log-step (Hillis-Steele) scan of the tile.
+// "Selective-scan CUDA kernels", the predictions: the page's Hillis-Steele
+// ran in PyTorch, which it notes is not a fair comparison with its
+// single-pass kernel. Here the same persistent look-back kernel runs with
+// the tile scanned by the log-step algorithm instead: each thread keeps its
+// 16 elements in registers; in step k every element E >= 2^k is combined
+// with element E - 2^k as it was after step k-1, the values passing through
+// the tile's shared-memory buffer; 12 steps for 4096 elements (work
+// O(n log n) instead of O(n)). The tile buffer ends up holding every
+// element's inclusive pair from the tile start, and the fix-up is one fma.
+__device__ __forceinline__ void scan_tile_hs(const AffineParams &p, unsigned tile, unsigned tag,
+                                             float *s_a, float *s_b, uint64_t *bar, unsigned use,
+                                             Pair *s_tagg) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long rem = p.n - (long long)tile * kTile;
+    if (p.bulk_ok && rem >= kTile) {
+        const unsigned parity = use & 1u;
+        if (!mbar_wait_bounded(bar, parity, kCopyTimeoutNs)) {
+            record_error(p.ws, SS_ERR_TIMEOUT, 1u, tile, 0u);
+            mbar_wait_bounded(bar, parity, kCopyTimeoutNs);
+        }
+    }
+    compute_sync();
+    float a[kItems], b[kItems];
+#pragma unroll
+    for (int j = 0; j < kStripes; ++j) {
+        const int off = warp * kWarpElems + j * 128 + lane * 4;
+        const float4 va = *reinterpret_cast<const float4 *>(&s_a[off]);
+        const float4 vb = *reinterpret_cast<const float4 *>(&s_b[off]);
+        a[4 * j] = va.x; a[4 * j + 1] = va.y; a[4 * j + 2] = va.z; a[4 * j + 3] = va.w;
+        b[4 * j] = vb.x; b[4 * j + 1] = vb.y; b[4 * j + 2] = vb.z; b[4 * j + 3] = vb.w;
+    }
+    for (int o = 1; o < kTile; o <<= 1) {
+        float pa[kItems], pb[kItems];  // element E - o after the previous step
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            const int E = warp * kWarpElems + (k >> 2) * 128 + lane * 4 + (k & 3);
+            pa[k] = E >= o ? s_a[E - o] : 1.0f;
+            pb[k] = E >= o ? s_b[E - o] : 0.0f;
+        }
+        compute_sync();  // every partner is read before any is overwritten
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            const Pair c = compose({pa[k], pb[k]}, {a[k], b[k]});
+            a[k] = c.a;
+            b[k] = c.b;
+        }
+#pragma unroll
+        for (int j = 0; j < kStripes; ++j) {
+            const int off = warp * kWarpElems + j * 128 + lane * 4;
+            *reinterpret_cast<float4 *>(&s_a[off]) = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+            *reinterpret_cast<float4 *>(&s_b[off]) = make_float4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+        }
+        compute_sync();  // this step's values are in place
+    }
+    if (tid == 0) {
+        const Pair tagg = {s_a[kTile - 1], s_b[kTile - 1]};
+        *s_tagg = tagg;
+        if ((long long)tile != p.skip_unit) {
+            TileDesc *d = p.desc + tile;
+            st_relaxed_u64(&d->agg_a, pack_tagged(tag, tagg.a));
+            st_relaxed_u64(&d->agg_b, pack_tagged(tag, tagg.b));
+            if (tile == 0) st_relaxed_u64(&d->inc, pack_tagged(tag, tagg.b));
+        }
+    }
+}
+
+// Fix-up of the log-step variant: h = A_E * carry + B_E from the tile
+// buffer's inclusive pairs.
+__device__ __forceinline__ void fix_up_hs(const AffineParams &p, unsigned tile, const float *s_a,
+                                          const float *s_b, float carry) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long base = (long long)tile * kTile;
+    const long long rem = p.n - base;
+    const int valid = rem >= kTile ? kTile : (int)rem;
+#pragma unroll
+    for (int j = 0; j < kStripes; ++j) {
+        const int off = warp * kWarpElems + j * 128 + lane * 4;
+        const float4 va = *reinterpret_cast<const float4 *>(&s_a[off]);
+        const float4 vb = *reinterpret_cast<const float4 *>(&s_b[off]);
+        const float4 o = make_float4(fmaf(va.x, carry, vb.x), fmaf(va.y, carry, vb.y),
+                                     fmaf(va.z, carry, vb.z), fmaf(va.w, carry, vb.w));
+        const long long g = base + off;
+        if (p.vec_out && off + 4 <= valid) {
+            __stcs(reinterpret_cast<float4 *>(p.h + g), o);
+        } else {
+            if (off + 0 < valid) p.h[g + 0] = o.x;
+            if (off + 1 < valid) p.h[g + 1] = o.y;
+            if (off + 2 < valid) p.h[g + 2] = o.z;
+            if (off + 3 < valid) p.h[g + 3] = o.w;
+        }
+    }
+}
+
 // Control warp: the state entering `tile` (nearest published inclusive state,
 // then the aggregates after it applied in sequence order); publishes the
 // tile's inclusive state and leaves the carry in *s_carry.
@@ -417,10 +511,25 @@ __device__ __forceinline__ void control_loop(const AffineParams &p, AffineShared
 // fix up and store tile q and restage its buffer. Two steps per loop trip so
 // the two scan results swap roles without indexing (tile q's results are in
 // rc for even q, in rn for odd q).
+template <bool HS>
 __device__ __forceinline__ void compute_loop(const AffineParams &p, AffineShared &sh, float *s_dyn,
                                              unsigned num_tiles) {
     const unsigned tag = sh.tag;
     auto abuf = [&](unsigned q) { return s_dyn + (q % kBufs) * (2 * kTile); };
+    // CTA-local tile q: staged in buffer q % kBufs, its load number q / kBufs
+    auto scan = [&](unsigned tile, unsigned q, Pair *tagg, TileScan &r) {
+        if constexpr (HS)
+            scan_tile_hs(p, tile, tag, abuf(q), abuf(q) + kTile, &sh.bar[q % kBufs], q / kBufs, tagg);
+        else
+            scan_tile(p, tile, tag, abuf(q), abuf(q) + kTile, &sh.bar[q % kBufs], q / kBufs,
+                      sh.warp_agg, tagg, r);
+    };
+    auto fix = [&](unsigned tile, unsigned q, const TileScan &r) {
+        if constexpr (HS)
+            fix_up_hs(p, tile, abuf(q), abuf(q) + kTile, sh.carry);
+        else
+            fix_up(p, tile, abuf(q), abuf(q) + kTile, r, sh.carry);
+    };
     unsigned cur = sh.tick[0], nxt = sh.tick[1];
     for (int i = 0; i < kBufs; ++i) {
         const unsigned t = sh.tick[i];
@@ -428,15 +537,14 @@ __device__ __forceinline__ void compute_loop(const AffineParams &p, AffineShared
     }
     TileScan rc, rn;
     if (cur < num_tiles)
-        scan_tile(p, cur, tag, abuf(0), abuf(0) + kTile, &sh.bar[0], 0u, sh.warp_agg, &sh.tagg[0], rc);
+        scan(cur, 0, &sh.tagg[0], rc);
     __syncthreads();  // tile 0's aggregate is visible to the control warp
     for (unsigned q = 0; cur < num_tiles; q += 2) {
         if (nxt < num_tiles)
-            scan_tile(p, nxt, tag, abuf(q + 1), abuf(q + 1) + kTile, &sh.bar[(q + 1) % kBufs],
-                      (q + 1) / kBufs, sh.warp_agg, &sh.tagg[1], rn);
+            scan(nxt, q + 1, &sh.tagg[1], rn);
         __syncthreads();
         unsigned after = sh.tick[(q + kBufs) % kTicks];
-        fix_up(p, cur, abuf(q), abuf(q) + kTile, rc, sh.carry);
+        fix(cur, q, rc);
         compute_sync();  // tile q's buffer is free
         if (after < num_tiles) stage_tile(p, after, abuf(q), abuf(q) + kTile, &sh.bar[q % kBufs]);
         __syncthreads();
@@ -446,11 +554,10 @@ __device__ __forceinline__ void compute_loop(const AffineParams &p, AffineShared
 
         const unsigned q1 = q + 1;
         if (nxt < num_tiles)
-            scan_tile(p, nxt, tag, abuf(q1 + 1), abuf(q1 + 1) + kTile, &sh.bar[(q1 + 1) % kBufs],
-                      (q1 + 1) / kBufs, sh.warp_agg, &sh.tagg[0], rc);
+            scan(nxt, q1 + 1, &sh.tagg[0], rc);
         __syncthreads();
         after = sh.tick[(q1 + kBufs) % kTicks];
-        fix_up(p, cur, abuf(q1), abuf(q1) + kTile, rn, sh.carry);
+        fix(cur, q1, rn);
         compute_sync();
         if (after < num_tiles) stage_tile(p, after, abuf(q1), abuf(q1) + kTile, &sh.bar[q1 % kBufs]);
         __syncthreads();
@@ -468,6 +575,7 @@ __device__ __forceinline__ void compute_loop(const AffineParams &p, AffineShared
 // q+kBufs. A tile's aggregate never waits on another tile's look-back, and
 // the look-back overlaps the scan. Both loops pass the same two barriers per
 // step and stop at the same step.
+template <bool HS>
 __global__ void __launch_bounds__(kCtaThreads, kBufs == 2 ? 3 : 2)
 affine_scan_kernel(const AffineParams p) {
     extern __shared__ __align__(128) float s_dyn[];  // [kBufs][a | b][kTile]
@@ -485,7 +593,7 @@ affine_scan_kernel(const AffineParams p) {
     if (threadIdx.x >= kThreads)
         control_loop(p, sh, s_walk, num_tiles);
     else
-        compute_loop(p, sh, s_dyn, num_tiles);
+        compute_loop<HS>(p, sh, s_dyn, num_tiles);
     finish_launch(p.ws, sh.tag);
 }
 
@@ -497,8 +605,34 @@ size_t affine_workspace_bytes(int64_t n) {
     return kWsHeaderBytes + (size_t)tiles * sizeof(TileDesc);
 }
 
+namespace {
+
+template <bool HS>
+ss_status launch_variant(const AffineParams &prm, int64_t tiles, cudaStream_t stream) {
+    // persistent grid: as many CTAs as fit at once, capped by the tile count
+    static int ctas_per_sm = -1, sms = 0;
+    if (ctas_per_sm < 0) {
+        int dev = 0, per_sm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaFuncSetAttribute(affine_scan_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kDynSmem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, affine_scan_kernel<HS>,
+                                                          kCtaThreads, kDynSmem) != cudaSuccess ||
+            per_sm < 1)
+            return SS_ERR_CUDA;
+        ctas_per_sm = per_sm;
+    }
+    const long long grid = std::min<long long>(tiles, (long long)sms * ctas_per_sm);
+    affine_scan_kernel<HS><<<(unsigned)grid, kCtaThreads, kDynSmem, stream>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
+}  // namespace
+
 ss_status affine_launch(const float *a, const float *b, float *h, int64_t n, void *workspace,
-                        cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit) {
+                        cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit,
+                        bool log_step_tiles) {
     const int64_t tiles = (n + kTile - 1) / kTile;
     if (tiles > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
     AffineParams prm;
@@ -512,23 +646,8 @@ ss_status affine_launch(const float *a, const float *b, float *h, int64_t n, voi
     prm.skip_unit = skip_unit;
     prm.bulk_ok = ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
     prm.vec_out = (reinterpret_cast<uintptr_t>(h) & 15u) == 0;
-    // persistent grid: as many CTAs as fit at once, capped by the tile count
-    static int ctas_per_sm = -1, sms = 0;
-    if (ctas_per_sm < 0) {
-        int dev = 0, per_sm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaFuncSetAttribute(affine_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDynSmem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, affine_scan_kernel, kCtaThreads,
-                                                          kDynSmem) != cudaSuccess ||
-            per_sm < 1)
-            return SS_ERR_CUDA;
-        ctas_per_sm = per_sm;
-    }
-    const long long grid = std::min<long long>(tiles, (long long)sms * ctas_per_sm);
-    affine_scan_kernel<<<(unsigned)grid, kCtaThreads, kDynSmem, stream>>>(prm);
-    return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    return log_step_tiles ? launch_variant<true>(prm, tiles, stream)
+                          : launch_variant<false>(prm, tiles, stream);
 }
 
 }  // namespace ss

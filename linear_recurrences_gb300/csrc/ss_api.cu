@@ -54,6 +54,18 @@ ss_status s6_entry(const void *x, const void *delta, const void *Bt, const void 
                          g_timeout_ns.load(), take_skip_unit());
 }
 
+ss_status affine_entry(const float *a, const float *b, float *h, int64_t n, void *workspace,
+                       size_t workspace_bytes, void *stream, bool log_step) {
+    if (n < 0) return SS_ERR_INVALID;
+    if (n == 0) return SS_OK;
+    if (!a || !b || !h) return SS_ERR_INVALID;
+    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(h, 4)) return SS_ERR_INVALID;
+    const size_t need = ss::affine_workspace_bytes(n);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SS_ERR_WORKSPACE;
+    return ss::affine_launch(a, b, h, n, workspace, static_cast<cudaStream_t>(stream),
+                             g_timeout_ns.load(), take_skip_unit(), log_step);
+}
+
 }  // namespace
 
 namespace ss {
@@ -81,14 +93,12 @@ size_t ss_affine_scan_workspace_bytes(int64_t n) { return ss::affine_workspace_b
 
 ss_status ss_affine_scan(const float *a, const float *b, float *h, int64_t n, void *workspace,
                          size_t workspace_bytes, void *stream) {
-    if (n < 0) return SS_ERR_INVALID;
-    if (n == 0) return SS_OK;
-    if (!a || !b || !h) return SS_ERR_INVALID;
-    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(h, 4)) return SS_ERR_INVALID;
-    const size_t need = ss::affine_workspace_bytes(n);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SS_ERR_WORKSPACE;
-    return ss::affine_launch(a, b, h, n, workspace, static_cast<cudaStream_t>(stream),
-                             g_timeout_ns.load(), take_skip_unit());
+    return affine_entry(a, b, h, n, workspace, workspace_bytes, stream, false);
+}
+
+ss_status ss_affine_scan_log_step(const float *a, const float *b, float *h, int64_t n,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    return affine_entry(a, b, h, n, workspace, workspace_bytes, stream, true);
 }
 
 size_t ss_selective_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,

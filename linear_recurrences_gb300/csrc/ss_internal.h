@@ -10,8 +10,11 @@
 namespace ss {
 
 size_t affine_workspace_bytes(int64_t n);
+// log_step_tiles: scan each tile with the log-step (Hillis-Steele) algorithm
+// instead of the work-efficient register scan (comparison variant).
 ss_status affine_launch(const float *a, const float *b, float *h, int64_t n, void *workspace,
-                        cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit);
+                        cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit,
+                        bool log_step_tiles = false);
 
 struct S6Args {
     const void *x, *delta, *Bt, *Ct;
