@@ -117,3 +117,15 @@ def test_bwd_workload_fp32(torch, ss):
     got = gpu_bwd(ss, torch, inp, dy, None, None, w.softplus)
     ref = oracle_bwd(inp, dy, None, None, w.softplus)
     check(got, ref, "f32")
+
+
+def test_bwd_workload_bf16(torch, ss):
+    """The bf16 S6 workload (B8 L4096 D1536 N16, softplus) in the benchmark's
+    configuration, every gradient compared."""
+    w = workloads.S6["s6_bf16"]
+    inp = workloads.s6_workload_inputs(w)
+    g = np.random.Generator(np.random.PCG64(17))
+    dys = workloads.f32_to_bf16_bits(g.standard_normal((w.B, w.L, w.D)).astype(np.float32))
+    got = gpu_bwd(ss, torch, inp, dys, None, None, w.softplus)
+    ref = oracle_bwd(inp, workloads.bf16_bits_to_f32(dys), None, None, w.softplus)
+    check(got, ref, "bf16")

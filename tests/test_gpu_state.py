@@ -132,3 +132,19 @@ def test_state_workload_full(torch, ss):
     ry, rhl = oracle_state(inp, h0.astype(np.float64), w.softplus)
     assert rel_err(y, ry) <= TOL["f32"]
     assert rel_err(hl, rhl) <= TOL_STATE["f32"]
+
+
+def test_state_workload_bf16_first_batch(torch, ss):
+    """The bf16 S6 workload (B8 L4096 D1536 N16, softplus) from a random h0, in
+    the benchmark's configuration; batch element 0 (which depends on nothing
+    else) compared in full, y and h_last."""
+    w = workloads.S6["s6_bf16"]
+    inp = workloads.s6_workload_inputs(w)
+    h0 = np.random.Generator(np.random.PCG64(7)).standard_normal((w.B, w.D, w.N)).astype(np.float32)
+    y, hl = gpu_state(ss, torch, inp, h0, w.softplus)
+    one = lambda v: np.ascontiguousarray(v[:1])
+    ry, rhl = oracle.s6_fwd_state(one(inp.x_f32), one(inp.delta_f32), one(inp.Bt_f32),
+                                  one(inp.Ct_f32), inp.A, inp.Dskip, h0=h0[:1].astype(np.float64),
+                                  softplus=True, threads=THREADS)
+    assert rel_err(y[:1], ry) <= TOL["bf16"]
+    assert rel_err(hl[:1], rhl) <= TOL_STATE["bf16"]
