@@ -59,6 +59,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     i64 = ctypes.c_int64
     lib.oracle_affine_f64.argtypes = [f, f, dp, i64]
     lib.oracle_affine_f64.restype = None
+    lib.oracle_affine_state_f64.argtypes = [f, f, ctypes.c_double, dp, i64]
+    lib.oracle_affine_state_f64.restype = None
     lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
     lib.oracle_softplus_f64.restype = ctypes.c_double
     s6 = [f, f, f, f, f, f, dp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int]
@@ -91,14 +93,18 @@ def _p(a, t=ctypes.c_float):
 
 
 # ---------------------------------------------------------------- affine
-def affine(a, b, lib: ctypes.CDLL | None = None) -> np.ndarray:
-    """h[t] = a[t]*h[t-1] + b[t], h[-1] = 0, in float64."""
+def affine(a, b, lib: ctypes.CDLL | None = None, h0: float | None = None) -> np.ndarray:
+    """h[t] = a[t]*h[t-1] + b[t], in float64, from h[-1] = 0, or from h[-1] =
+    h0 (a scan continued from an earlier segment's last state)."""
     lib = lib or load()
     a, b = _f32(a), _f32(b)
     if a.shape != b.shape or a.ndim != 1:
         raise ValueError("a and b must be 1-D of equal length")
     h = np.empty(a.shape[0], dtype=np.float64)
-    lib.oracle_affine_f64(_p(a), _p(b), _p(h, ctypes.c_double), a.shape[0])
+    if h0 is None:
+        lib.oracle_affine_f64(_p(a), _p(b), _p(h, ctypes.c_double), a.shape[0])
+    else:
+        lib.oracle_affine_state_f64(_p(a), _p(b), float(h0), _p(h, ctypes.c_double), a.shape[0])
     return h
 
 

@@ -25,7 +25,9 @@
  *          equal the two scans run independently.
  *
  * Readings where the pages are silent (each is listed in the design notes):
- *   - h[-1] = 0 for the affine scan; h starts at 0 for S6 ([S6]).
+ *   - h[-1] = 0 for the affine scan; h starts at 0 for S6 ([S6]). A scan
+ *     continued from an earlier segment starts from that segment's last
+ *     state h0 instead.
  *   - softplus uses threshold 20: v > 20 returns v (PyTorch's default).
  *   - the reverse recurrence applies dA and dBx of the same time index:
  *     h_rev[t] = dA[t]*h_rev[t+1] + dBx[t], i.e. the forward scan of the
@@ -43,14 +45,21 @@
 
 /* ------------------------------------------------------------------ affine */
 
-/* [SSK] h[t] = a[t]*h[t-1] + b[t], with h[-1] = 0. */
-void oracle_affine_f64(const float *a, const float *b, double *h, int64_t n)
+/* [SSK] h[t] = a[t]*h[t-1] + b[t], with h[-1] = h0 (the reading for a
+ * scan continued from an earlier segment: h0 is that segment's last state). */
+void oracle_affine_state_f64(const float *a, const float *b, double h0, double *h, int64_t n)
 {
-    double state = 0.0;
+    double state = h0;
     for (int64_t t = 0; t < n; ++t) {
         state = (double)a[t] * state + (double)b[t];
         h[t] = state;
     }
+}
+
+/* [SSK] h[t] = a[t]*h[t-1] + b[t], with h[-1] = 0. */
+void oracle_affine_f64(const float *a, const float *b, double *h, int64_t n)
+{
+    oracle_affine_state_f64(a, b, 0.0, h, n);
 }
 
 /* ------------------------------------------------------------------ S6 */

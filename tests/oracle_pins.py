@@ -166,10 +166,51 @@ def pin_affine_edges(lib):
     assert h[0] == -2.5
 
 
+def pin_affine_state_prepend(lib):
+    """Starting from h0 is the plain scan of the sequence with one element
+    (a = 0, b = h0) put in front: exact, since the arithmetic is the same."""
+    g = _rng(7)
+    for n in (1, 5, 33):
+        a = _dyadic(g, n, -1.0, 1.0, 4)
+        b = _dyadic(g, n, -2.0, 2.0, 4)
+        h0 = float(_dyadic(g, 1, -4.0, 4.0, 4)[0])
+        h = oracle.affine(a, b, lib=lib, h0=h0)
+        longer = oracle.affine(np.concatenate([np.zeros(1, np.float32), a]),
+                               np.concatenate([np.array([h0], np.float32), b]), lib=lib)
+        assert np.array_equal(h, longer[1:]), "h0 start differs from a prepended element"
+
+
+def pin_affine_state_closed_form(lib):
+    """a == c, b == 1 from h0: h[t] = c^(t+1) h0 + (1 - c^(t+1)) / (1 - c)."""
+    c, h0, n = 0.75, -3.0, 200
+    h = oracle.affine(np.full(n, c, np.float32), np.ones(n, np.float32), lib=lib, h0=h0)
+    t = np.arange(n)
+    closed = c ** (t + 1) * h0 + (1.0 - c ** (t + 1)) / (1.0 - c)
+    assert _rel(h, closed) < 1e-12, "closed form from h0"
+    # c = 1/2: every power is exact, so the decay of h0 must be too
+    h = oracle.affine(np.full(n, 0.5, np.float32), np.zeros(n, np.float32), lib=lib, h0=h0)
+    assert np.array_equal(h, 0.5 ** (t + 1) * h0), "pure decay of h0"
+
+
+def pin_affine_state_split(lib):
+    """Scanning [0, k) and then [k, n) from the first part's last state is the
+    same loop as scanning [0, n) in one go: bitwise equal."""
+    g = _rng(8)
+    n = 1000
+    a = g.uniform(0.9, 1.0, n).astype(np.float32)
+    b = g.standard_normal(n).astype(np.float32)
+    whole = oracle.affine(a, b, lib=lib)
+    for k in (1, 17, 500, 999):
+        first = oracle.affine(a[:k], b[:k], lib=lib)
+        second = oracle.affine(a[k:], b[k:], lib=lib, h0=first[-1])
+        assert np.array_equal(np.concatenate([first, second]), whole), f"split at {k}"
+
+
 AFFINE_PINS = [pin_affine_ones_integer, pin_affine_zero, pin_affine_geometric,
                pin_affine_power_sum, pin_affine_bracketings,
                pin_affine_swapped_combine_is_caught, pin_affine_impulse,
-               pin_affine_edges]
+               pin_affine_edges, pin_affine_state_prepend, pin_affine_state_closed_form,
+               pin_affine_state_split]
 
 
 # ---------------------------------------------------------------- S6 pins

@@ -21,6 +21,11 @@ MUTANTS = [
     ("affine_store_before_update",
      "state = (double)a[t] * state + (double)b[t];\n        h[t] = state;",
      "h[t] = state;\n        state = (double)a[t] * state + (double)b[t];", 1),
+    ("affine_h0_ignored",
+     "double state = h0;", "double state = 0.0;", 1),
+    ("affine_h0_added_after_first_step",
+     "double state = h0;\n    for (int64_t t = 0; t < n; ++t) {\n        state = (double)a[t] * state + (double)b[t];",
+     "double state = 0.0;\n    for (int64_t t = 0; t < n; ++t) {\n        state = (double)a[t] * state + (double)b[t] + (t == 0 ? h0 : 0.0);", 1),
     ("s6_dropped_skip_term",
      "y[t * ystride] = acc + xv * Dd;", "y[t * ystride] = acc;", 1),
     ("s6_exp_sign",
