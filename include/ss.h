@@ -115,6 +115,45 @@ ss_status ss_affine_scan_log_step(const float *a, const float *b, float *h, int6
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * ss_affine_scan continued from a state: h[-1] = *h0 instead of 0, so a long
+ * sequence can be scanned segment by segment, each segment started from the
+ * previous one's last output ("Selective-scan CUDA kernels", opening
+ * paragraphs: the recurrence; its h[-1] is the state the segment inherits).
+ * h0: DEVICE pointer to one float, read by the kernel when it runs (so it may
+ * be written by earlier work on the same stream), or NULL for 0; it must not
+ * lie inside h (SS_ERR_INVALID). Workspace, results (deterministic) and
+ * errors as ss_affine_scan.
+ */
+ss_status ss_affine_scan_state(const float *a, const float *b, float *h, int64_t n,
+                               const float *h0, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* Bytes of DEVICE workspace ss_affine_scan_host needs for n elements (0 for
+ * n <= 0): the scan's own workspace plus three device slots of a, b and h
+ * for one chunk each. */
+size_t ss_affine_scan_host_workspace_bytes(int64_t n);
+
+/*
+ * The affine scan of HOST arrays: a, b (inputs) and h (output) are host
+ * pointers, best page-locked (cudaHostAlloc / cudaHostRegister), else the
+ * copies are staged by the driver and do not overlap. The input is cut into
+ * chunks of 2^23 elements; each chunk is copied into a device slot of the
+ * workspace, scanned there from the previous chunk's last state (the
+ * ss_affine_scan_state kernel) and copied back, with the copies towards the
+ * device, the scans and the copies back on three streams so the two
+ * directions of the host link and the GPU all work at once. Same h as the
+ * recurrence from h[-1] = 0, up to rounding order (deterministic for a
+ * given n). workspace: DEVICE memory of ss_affine_scan_host_workspace_bytes
+ * (n) bytes, zero-filled before first use like every workspace. The call
+ * returns once everything is enqueued; `stream` then waits for the last copy
+ * back, so h is complete when `stream` is. Calls on the same device are
+ * serialised while they enqueue (the library's two copy streams and their
+ * events are shared); the arrays must stay valid until then.
+ */
+ss_status ss_affine_scan_host(const float *a, const float *b, float *h, int64_t n,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Largest n ss_affine_scan_noalloc accepts (2^24 elements). Its scratch
  * array is 256 + 32 * (SS_AFFINE_NOALLOC_MAX_N / 4096) = 131,328 bytes.
  */

@@ -29,7 +29,8 @@ __all__ = [
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
     "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
     "ss_selective_scan_layer_fwd", "ss_selective_scan_layer_workspace_bytes",
-    "ss_affine_scan_log_step", "new_workspace", "EXPORTED_SYMBOLS",
+    "ss_affine_scan_log_step", "ss_affine_scan_state", "ss_affine_scan_host",
+    "ss_affine_scan_host_workspace_bytes", "new_workspace", "EXPORTED_SYMBOLS",
 ]
 
 SS_OK, SS_ERR_INVALID, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -43,7 +44,8 @@ EXPORTED_SYMBOLS = (
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_selective_scan_fwd_state",
     "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
     "ss_selective_scan_layer_workspace_bytes", "ss_selective_scan_layer_fwd",
-    "ss_affine_scan_log_step",
+    "ss_affine_scan_log_step", "ss_affine_scan_state", "ss_affine_scan_host_workspace_bytes",
+    "ss_affine_scan_host",
 )
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -116,6 +118,12 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_selective_scan_layer_fwd.restype = ci
     L.ss_affine_scan_log_step.argtypes = [vp, vp, vp, i64, vp, sz, vp]
     L.ss_affine_scan_log_step.restype = ci
+    L.ss_affine_scan_state.argtypes = [vp, vp, vp, i64, vp, vp, sz, vp]
+    L.ss_affine_scan_state.restype = ci
+    L.ss_affine_scan_host_workspace_bytes.argtypes = [i64]
+    L.ss_affine_scan_host_workspace_bytes.restype = sz
+    L.ss_affine_scan_host.argtypes = [vp, vp, vp, i64, vp, sz, vp]
+    L.ss_affine_scan_host.restype = ci
     return L
 
 
@@ -231,6 +239,78 @@ def ss_affine_scan_log_step(a, b, h=None, workspace=None, stream=None):
     """The affine scan with a log-step (Hillis-Steele) scan of each tile: a
     comparison kernel for the work-efficient ss_affine_scan."""
     return ss_affine_scan(a, b, h, workspace, stream, _fn="ss_affine_scan_log_step")
+
+
+def ss_affine_scan_state(a, b, h0=None, h=None, workspace=None, stream=None):
+    """The affine scan from h[-1] = h0: h0 is a 1-element fp32 CUDA tensor
+    (read when the kernel runs) or None for 0. Returns h."""
+    torch = _torch()
+    _check_cuda(a, "a", (torch.float32,))
+    _check_cuda(b, "b", (torch.float32,))
+    if a.dim() != 1 or a.shape != b.shape or a.device != b.device:
+        raise ValueError("a and b must be 1-D, same length, same device")
+    if h0 is not None:
+        _check_cuda(h0, "h0", (torch.float32,))
+        if h0.numel() != 1 or h0.device != a.device:
+            raise ValueError("h0 must hold one float on a's device")
+    n = a.numel()
+    if h is None:
+        h = torch.empty_like(a)
+    _check_cuda(h, "h", (torch.float32,))
+    if h.shape != a.shape:
+        raise ValueError("h must match a")
+    sh = _stream_handle(stream, a.device)
+    need = ss_affine_scan_workspace_bytes(n)
+    if workspace is None and need:
+        workspace = _cached_workspace(("affine_state",), need, a.device, sh)
+    wsb = workspace.numel() if workspace is not None else 0
+    st = lib().ss_affine_scan_state(_ptr(a), _ptr(b), _ptr(h), n, _ptr(h0), _ptr(workspace),
+                                    wsb, sh)
+    if st != SS_OK:
+        raise SSError(st, "ss_affine_scan_state")
+    return h
+
+
+def ss_affine_scan_host_workspace_bytes(n: int) -> int:
+    return lib().ss_affine_scan_host_workspace_bytes(int(n))
+
+
+def _check_host(t, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda or not t.is_contiguous() or t.dtype != torch.float32 or t.dim() != 1:
+        raise ValueError(f"{name} must be a contiguous 1-D float32 host tensor")
+
+
+def ss_affine_scan_host(a, b, h=None, workspace=None, stream=None, device=None):
+    """The affine scan of HOST tensors (best pinned: torch's pin_memory()),
+    streamed through the GPU in chunks with copies in both directions
+    overlapping the scans. Returns h (a host tensor); it is complete once
+    `stream` (default: the current stream of `device`) is."""
+    torch = _torch()
+    _check_host(a, "a")
+    _check_host(b, "b")
+    if a.shape != b.shape:
+        raise ValueError("a and b must have the same length")
+    n = a.numel()
+    if h is None:
+        h = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    _check_host(h, "h")
+    if h.shape != a.shape:
+        raise ValueError("h must match a")
+    dev = torch.device(device) if device is not None else (
+        workspace.device if workspace is not None else torch.device("cuda", torch.cuda.current_device()))
+    sh = _stream_handle(stream, dev)
+    need = ss_affine_scan_host_workspace_bytes(n)
+    if workspace is None and need:
+        workspace = _cached_workspace(("affine_host",), need, dev, sh)
+    wsb = workspace.numel() if workspace is not None else 0
+    with torch.cuda.device(dev):
+        st = lib().ss_affine_scan_host(_ptr(a), _ptr(b), _ptr(h), n, _ptr(workspace), wsb, sh)
+    if st != SS_OK:
+        raise SSError(st, "ss_affine_scan_host")
+    return h
 
 
 SS_AFFINE_NOALLOC_MAX_N = 1 << 24

@@ -92,6 +92,7 @@ struct AffineParams {
     const float *a;
     const float *b;
     float *h;
+    const float *h0;  // state before element 0 (one float), or null for 0
     long long n;
     WsHeader *ws;
     TileDesc *desc;
@@ -208,7 +209,9 @@ __device__ __forceinline__ void scan_tile(const AffineParams &p, unsigned tile, 
             TileDesc *d = p.desc + tile;
             st_relaxed_u64(&d->agg_a, pack_tagged(tag, r.tagg.a));
             st_relaxed_u64(&d->agg_b, pack_tagged(tag, r.tagg.b));
-            if (tile == 0) st_relaxed_u64(&d->inc, pack_tagged(tag, r.tagg.b));
+            // tile 0's inclusive state; from an initial state the control
+            // warp publishes it with the carry instead
+            if (tile == 0 && !p.h0) st_relaxed_u64(&d->inc, pack_tagged(tag, r.tagg.b));
         }
     }
     compute_sync();  // s_warp is free for the next tile
@@ -276,7 +279,7 @@ __device__ __forceinline__ void scan_tile_hs(const AffineParams &p, unsigned til
             TileDesc *d = p.desc + tile;
             st_relaxed_u64(&d->agg_a, pack_tagged(tag, tagg.a));
             st_relaxed_u64(&d->agg_b, pack_tagged(tag, tagg.b));
-            if (tile == 0) st_relaxed_u64(&d->inc, pack_tagged(tag, tagg.b));
+            if (tile == 0 && !p.h0) st_relaxed_u64(&d->inc, pack_tagged(tag, tagg.b));
         }
     }
 }
@@ -318,7 +321,9 @@ __device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, 
                                           const Pair &tagg, Pair *s_walk, float *s_carry) {
     const int lane = threadIdx.x & 31;
     float e = 0.0f;
-    if (tile > 0) {
+    if (tile == 0) {
+        if (p.h0) e = *p.h0;
+    } else {
         int win = 0;
         int anchor_lane = -1;
         float anchor = 0.0f;
@@ -332,7 +337,8 @@ __device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, 
             Pair g[kPoll];
 #pragma unroll
             for (int i = 0; i < kPoll; ++i) {
-                // before tile 0: the state h[-1] = 0 counts as inclusive
+                // before tile 0: the state h[-1] counts as inclusive (0 here,
+                // h0 substituted once the anchor is chosen)
                 kind[i] = (long long)tile - 32LL * (win + 1 + i) + lane < 0 ? 2 : 0;
                 v[i] = 0.0f;
                 g[i] = {1.0f, 0.0f};
@@ -389,7 +395,10 @@ __device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, 
                     found = true;
                 }
             }
-            if (found) break;
+            if (found) {
+                if (p.h0 && (long long)tile - 32LL * (win + 1) + anchor_lane < 0) anchor = *p.h0;
+                break;
+            }
             if (win + kPoll < kMaxWindows) {
                 win += kPoll;
             } else if (globaltimer_ns() - walk_t0 > p.timeout_ns ||
@@ -435,7 +444,7 @@ __device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, 
     }
     if (lane == 0) {
         *s_carry = e;
-        if (tile > 0 && (long long)tile != p.skip_unit)
+        if ((tile > 0 || p.h0) && (long long)tile != p.skip_unit)
             st_relaxed_u64(&p.desc[tile].inc, pack_tagged(tag, apply(tagg, e)));
     }
     __syncwarp();
@@ -632,13 +641,14 @@ ss_status launch_variant(const AffineParams &prm, int64_t tiles, cudaStream_t st
 
 ss_status affine_launch(const float *a, const float *b, float *h, int64_t n, void *workspace,
                         cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit,
-                        bool log_step_tiles) {
+                        bool log_step_tiles, const float *h0) {
     const int64_t tiles = (n + kTile - 1) / kTile;
     if (tiles > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
     AffineParams prm;
     prm.a = a;
     prm.b = b;
     prm.h = h;
+    prm.h0 = h0;
     prm.n = n;
     prm.ws = reinterpret_cast<WsHeader *>(workspace);
     prm.desc = reinterpret_cast<TileDesc *>(reinterpret_cast<char *>(workspace) + kWsHeaderBytes);

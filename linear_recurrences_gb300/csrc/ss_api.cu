@@ -55,15 +55,18 @@ ss_status s6_entry(const void *x, const void *delta, const void *Bt, const void 
 }
 
 ss_status affine_entry(const float *a, const float *b, float *h, int64_t n, void *workspace,
-                       size_t workspace_bytes, void *stream, bool log_step) {
+                       size_t workspace_bytes, void *stream, bool log_step,
+                       const float *h0 = nullptr) {
     if (n < 0) return SS_ERR_INVALID;
     if (n == 0) return SS_OK;
     if (!a || !b || !h) return SS_ERR_INVALID;
-    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(h, 4)) return SS_ERR_INVALID;
+    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(h, 4) || (h0 && !aligned(h0, 4)))
+        return SS_ERR_INVALID;
+    if (h0 && h0 >= h && h0 < h + n) return SS_ERR_INVALID;  // the kernel writes h
     const size_t need = ss::affine_workspace_bytes(n);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SS_ERR_WORKSPACE;
     return ss::affine_launch(a, b, h, n, workspace, static_cast<cudaStream_t>(stream),
-                             g_timeout_ns.load(), take_skip_unit(), log_step);
+                             g_timeout_ns.load(), take_skip_unit(), log_step, h0);
 }
 
 }  // namespace
@@ -99,6 +102,27 @@ ss_status ss_affine_scan(const float *a, const float *b, float *h, int64_t n, vo
 ss_status ss_affine_scan_log_step(const float *a, const float *b, float *h, int64_t n,
                                   void *workspace, size_t workspace_bytes, void *stream) {
     return affine_entry(a, b, h, n, workspace, workspace_bytes, stream, true);
+}
+
+ss_status ss_affine_scan_state(const float *a, const float *b, float *h, int64_t n,
+                               const float *h0, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+    return affine_entry(a, b, h, n, workspace, workspace_bytes, stream, false, h0);
+}
+
+size_t ss_affine_scan_host_workspace_bytes(int64_t n) { return ss::affine_host_workspace_bytes(n); }
+
+ss_status ss_affine_scan_host(const float *a, const float *b, float *h, int64_t n,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    if (n < 0) return SS_ERR_INVALID;
+    if (n == 0) return SS_OK;
+    if (!a || !b || !h) return SS_ERR_INVALID;
+    if (!aligned(a, 4) || !aligned(b, 4) || !aligned(h, 4)) return SS_ERR_INVALID;
+    if (!workspace || workspace_bytes < ss::affine_host_workspace_bytes(n) ||
+        !aligned(workspace, 256))
+        return SS_ERR_WORKSPACE;
+    return ss::affine_host_launch(a, b, h, n, workspace, workspace_bytes,
+                                  static_cast<cudaStream_t>(stream), g_timeout_ns.load());
 }
 
 size_t ss_selective_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,

@@ -12,9 +12,17 @@ namespace ss {
 size_t affine_workspace_bytes(int64_t n);
 // log_step_tiles: scan each tile with the log-step (Hillis-Steele) algorithm
 // instead of the work-efficient register scan (comparison variant).
+// h0: device pointer to the state before element 0 (null: 0); must not lie
+// inside h.
 ss_status affine_launch(const float *a, const float *b, float *h, int64_t n, void *workspace,
                         cudaStream_t stream, unsigned long long timeout_ns, long long skip_unit,
-                        bool log_step_tiles = false);
+                        bool log_step_tiles = false, const float *h0 = nullptr);
+
+// Affine scan over host (or any UVA-addressable) buffers, pipelined through
+// device slots in the workspace; see ss_affine_scan_host.
+size_t affine_host_workspace_bytes(int64_t n);
+ss_status affine_host_launch(const float *a, const float *b, float *h, int64_t n, void *workspace,
+                             size_t ws_bytes, cudaStream_t stream, unsigned long long timeout_ns);
 
 struct S6Args {
     const void *x, *delta, *Bt, *Ct;

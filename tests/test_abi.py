@@ -58,6 +58,33 @@ def test_affine_argument_errors(L):
     assert L.ss_affine_scan(p, p, p, 0, None, 0, None) == ss.SS_OK  # empty: nothing to do
 
 
+def test_affine_state_and_host_argument_errors(L):
+    p = ctypes.c_void_p(256)
+    h = ctypes.c_void_p(4096)
+    inside = ctypes.c_void_p(4096 + 4 * 5)  # h0 at h[5]: the kernel would overwrite it
+    assert L.ss_affine_scan_state(p, p, h, 10, inside, p, 1 << 20, None) == ss.SS_ERR_INVALID
+    assert L.ss_affine_scan_state(p, p, h, 10, ctypes.c_void_p(258), p, 1 << 20, None) == \
+        ss.SS_ERR_INVALID
+    assert L.ss_affine_scan_state(p, p, h, -1, None, p, 1 << 20, None) == ss.SS_ERR_INVALID
+    assert L.ss_affine_scan_state(p, p, h, 10, None, None, 0, None) == ss.SS_ERR_WORKSPACE
+    assert L.ss_affine_scan_state(p, p, h, 0, None, None, 0, None) == ss.SS_OK
+    assert L.ss_affine_scan_host(p, p, h, -1, p, 1 << 30, None) == ss.SS_ERR_INVALID
+    assert L.ss_affine_scan_host(None, p, h, 10, p, 1 << 30, None) == ss.SS_ERR_INVALID
+    assert L.ss_affine_scan_host(p, p, h, 10, p, 64, None) == ss.SS_ERR_WORKSPACE
+    assert L.ss_affine_scan_host(p, p, h, 0, None, 0, None) == ss.SS_OK
+
+
+def test_affine_host_workspace_size(L):
+    """Scan workspace for one chunk (2^23 elements at most), then three slots
+    of a, b and h for one chunk each, every section 256-byte aligned."""
+    assert L.ss_affine_scan_host_workspace_bytes(0) == 0
+    assert L.ss_affine_scan_host_workspace_bytes(1) == 512 + 9 * 256
+    chunk = 1 << 23
+    full = (256 + 32 * (chunk // 4096)) + 9 * 4 * chunk
+    assert L.ss_affine_scan_host_workspace_bytes(chunk) == full
+    assert L.ss_affine_scan_host_workspace_bytes(1 << 28) == full
+
+
 def test_affine_workspace_size(L):
     assert L.ss_affine_scan_workspace_bytes(0) == 0
     assert L.ss_affine_scan_workspace_bytes(1) == 256 + 32
