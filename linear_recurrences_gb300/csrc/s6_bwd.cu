@@ -58,6 +58,7 @@ struct BwdParams {
     int SD;          // channel ranges (CTAs per (b, chunk))
     int Dr;          // channels per range (multiple of kWarps)
     int softplus;
+    int vec_rows;    // x, delta, dy, dx, ddelta 16-byte aligned with 16-byte rows
     // workspace, each [B][K][D][N] unless noted
     float *aggP, *aggH, *aggM;   // chunk aggregates
     float *carH, *carM;          // state entering / adjoint leaving each chunk
@@ -69,10 +70,6 @@ struct BwdParams {
 __device__ __forceinline__ float ld_io(const float *p, long long i) { return __ldg(p + i); }
 __device__ __forceinline__ float ld_io(const __nv_bfloat16 *p, long long i) {
     return __bfloat162float(p[i]);
-}
-__device__ __forceinline__ void st_io(float *p, long long i, float v) { p[i] = v; }
-__device__ __forceinline__ void st_io(__nv_bfloat16 *p, long long i, float v) {
-    p[i] = __float2bfloat16_rn(v);
 }
 
 // softplus(v) = log(1 + exp(v)), v > 20 passes through; the same MUFU form,
@@ -194,48 +191,162 @@ __device__ __forceinline__ void load_bc_tiles(const BwdParams &p, const ChunkCtx
     }
 }
 
-// This lane's 8 steps of channel d: discretisation step, x and dy (zeros for
-// steps past L or an absent channel, which makes every map the identity).
+// Row segments of kWarps consecutive channels (warp w takes channel
+// dbase + w) for the chunk's 256 steps go through shared memory, so global
+// memory sees whole segments: thread j moves step j's kWarps values of an
+// array with vector accesses (8 channels: 32 B in fp32, 16 B in bf16), where
+// the time-parallel layout would touch one cache line per lane and value.
+// Shared layout per array: [channel][kChunk], the value of step 8l + i (lane
+// l, item i) in slot i*32 + (l ^ 4i): a permutation within each item's row
+// under which both the staging threads (i = j % 8, l = j / 8) and the lanes
+// reading item i hit 32 distinct banks.
+__device__ __forceinline__ int stage_slot(int i, int l) { return i * 32 + (l ^ (4 * i)); }
+constexpr int kStageFloats = 3 * kWarps * kChunk;  // delta (as given), x, dy
+
+__device__ __forceinline__ void load8(const float *p, long long i, bool vec, int valid, float (&v)[8]) {
+    if (vec) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p + i));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p + i) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v[w] = w < valid ? __ldg(p + i + w) : 0.0f;
+    }
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, long long i, bool vec, int valid,
+                                      float (&v)[8]) {
+    if (vec) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p + i));
+        const unsigned w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[2 * k] = __uint_as_float(w4[k] << 16);
+            v[2 * k + 1] = __uint_as_float(w4[k] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v[w] = w < valid ? __bfloat162float(p[i + w]) : 0.0f;
+    }
+}
+__device__ __forceinline__ void store8(float *p, long long i, bool vec, int valid, const float (&v)[8]) {
+    if (vec) {
+        reinterpret_cast<float4 *>(p + i)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4 *>(p + i)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            if (w < valid) p[i + w] = v[w];
+    }
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, long long i, bool vec, int valid,
+                                       const float (&v)[8]) {
+    if (vec) {
+        unsigned w4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+            w4[k] = *reinterpret_cast<const unsigned *>(&b2);
+        }
+        *reinterpret_cast<uint4 *>(p + i) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            if (w < valid) p[i + w] = __float2bfloat16_rn(v[w]);
+    }
+}
+
+// Stages delta, x and dy of channels [dbase, dbase + kWarps) for the chunk
+// (zeros past L and past the range's last channel d1).
 template <typename IO>
-__device__ __forceinline__ void load_items(const BwdParams &p, const ChunkCtx &c, int d, bool dok,
-                                           int lane, float (&dl)[kItems], float (&x)[kItems],
-                                           float (&gy)[kItems], float (&v)[kItems]) {
-    const IO *xp = static_cast<const IO *>(p.x);
-    const IO *dp = static_cast<const IO *>(p.delta);
-    const IO *yp = static_cast<const IO *>(p.dy);
+__device__ __forceinline__ void stage_rows(const BwdParams &p, const ChunkCtx &c, int dbase,
+                                           float *stg) {
+    static_assert(kWarps == 8, "row segments of 8 channels");
+    const int j = threadIdx.x;
+    const long long t = c.t0 + j;
+    const int valid = min(kWarps, c.d1 - dbase);
+    const bool vec = p.vec_rows && valid == kWarps;
+    const int slot = stage_slot(j & (kItems - 1), j / kItems);
+    const void *src[3] = {p.delta, p.x, p.dy};
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        float v[8];
+        if (t < p.L)
+            load8(static_cast<const IO *>(src[a]), (c.b * p.L + t) * p.D + dbase, vec, valid, v);
+        else
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v[w] = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) stg[(a * kWarps + w) * kChunk + slot] = v[w];
+    }
+}
+
+// Writes dx (staged in the x array) and ddelta (staged in the delta array)
+// of channels [dbase, dbase + kWarps) that lie below d1.
+template <typename IO>
+__device__ __forceinline__ void store_rows(const BwdParams &p, const ChunkCtx &c, int dbase,
+                                           const float *stg) {
+    const int j = threadIdx.x;
+    const long long t = c.t0 + j;
+    if (t >= p.L) return;
+    const int valid = min(kWarps, c.d1 - dbase);
+    const bool vec = p.vec_rows && valid == kWarps;
+    const int slot = stage_slot(j & (kItems - 1), j / kItems);
+    const long long row = (c.b * p.L + t) * p.D + dbase;
+    float v[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v[w] = stg[(1 * kWarps + w) * kChunk + slot];
+    store8(static_cast<IO *>(p.dx), row, vec, valid, v);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) v[w] = stg[(0 * kWarps + w) * kChunk + slot];
+    store8(static_cast<IO *>(p.ddelta), row, vec, valid, v);
+}
+
+// This lane's 8 steps of the warp's staged channel: discretisation step, x,
+// dy and delta as given (zeros past L or for an absent channel, which makes
+// every map the identity).
+__device__ __forceinline__ void read_items(const BwdParams &p, const ChunkCtx &c, const float *stg,
+                                           bool dok, int warp, int lane, float (&dl)[kItems],
+                                           float (&x)[kItems], float (&gy)[kItems],
+                                           float (&v)[kItems]) {
 #pragma unroll
     for (int i = 0; i < kItems; ++i) {
-        const long long t = c.t0 + lane * kItems + i;
-        dl[i] = x[i] = gy[i] = v[i] = 0.0f;
-        if (dok && t < p.L) {
-            const long long g = (c.b * p.L + t) * p.D + d;
-            v[i] = ld_io(dp, g);
-            dl[i] = p.softplus ? softplus_fwd(v[i]) : v[i];
-            x[i] = ld_io(xp, g);
-            gy[i] = ld_io(yp, g);
-        }
+        const int s = stage_slot(i, lane);
+        v[i] = stg[(0 * kWarps + warp) * kChunk + s];
+        x[i] = stg[(1 * kWarps + warp) * kChunk + s];
+        gy[i] = stg[(2 * kWarps + warp) * kChunk + s];
+        const bool ok = dok && c.t0 + lane * kItems + i < p.L;  // else dA = 1: an identity step
+        dl[i] = ok ? (p.softplus ? softplus_fwd(v[i]) : v[i]) : 0.0f;
     }
 }
 
 // ---- launch 1: per (b, chunk, d, n) the product of dA, the forward end
 // state from zero, and the adjoint entering the chunk from zero.
+constexpr int kAggSmem = (2 * kMaxN * kChunk + kWarps * kMaxN + kStageFloats) * (int)sizeof(float);
+
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) bwd_aggregate_kernel(const BwdParams p) {
-    __shared__ float Bs[kMaxN * kChunk], Cs[kMaxN * kChunk];
-    __shared__ float sA[kWarps][kMaxN];
+    extern __shared__ __align__(16) float smem[];  // kAggSmem bytes
+    float *Bs = smem, *Cs = Bs + kMaxN * kChunk;
+    float *sA = Cs + kMaxN * kChunk;  // [warp][n]
+    float *stg = sA + kWarps * kMaxN;
     const ChunkCtx c = chunk_ctx(p);
     load_bc_tiles(p, c, Bs, Cs, sizeof(IO) == 2);
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int d = c.d0 + warp; d < c.d1; d += kWarps) {
-        if (lane < p.N) sA[warp][lane] = p.A[(long long)d * p.N + lane] * kLog2e;
+    for (int dbase = c.d0; dbase < c.d1; dbase += kWarps) {
+        const int d = dbase + warp;
+        const bool dok = d < c.d1;  // warp-uniform
+        if (dbase > c.d0) __syncthreads();  // the previous block's items are read
+        stage_rows<IO>(p, c, dbase, stg);
+        if (dok && lane < p.N) sA[warp * kMaxN + lane] = p.A[(long long)d * p.N + lane] * kLog2e;
+        __syncthreads();  // rows staged (and the first time the B, C tiles)
+        if (!dok) continue;
         float dl[kItems], x[kItems], gy[kItems], v[kItems];
-        load_items<IO>(p, c, d, true, lane, dl, x, gy, v);
+        read_items(p, c, stg, true, warp, lane, dl, x, gy, v);
 #pragma unroll
         for (int i = 0; i < kItems; ++i) x[i] *= dl[i];  // x now holds dl * x
-        __syncwarp();
         for (int n = 0; n < p.N; ++n) {
-            const float A2 = sA[warp][n];
+            const float A2 = sA[warp * kMaxN + n];
             float dA[kItems];
             Map f = {1.0f, 0.0f};
 #pragma unroll
@@ -255,7 +366,6 @@ __global__ void __launch_bounds__(kThreads) bwd_aggregate_kernel(const BwdParams
                 p.aggM[idx] = r.b;
             }
         }
-        __syncwarp();  // sA is rewritten for the next channel
     }
 }
 
@@ -285,7 +395,8 @@ __global__ void bwd_carry_kernel(const BwdParams p) {
 }
 
 constexpr int kGradSmem =
-    ((4 * kMaxN + 2 * kWarps) * kChunk + kWarps * 3 * kMaxN) * (int)sizeof(float);  // 81.5 KB
+    ((4 * kMaxN + 2 * kWarps) * kChunk + kWarps * 3 * kMaxN + kStageFloats) *
+    (int)sizeof(float);  // 105.5 KB
 
 // ---- launch 3: gradients of one chunk for a channel range. Warp w takes
 // channels d0 + w, d0 + w + 8, ...; per state n each warp rebuilds h over its
@@ -301,14 +412,13 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
     float *accB = Cs + kMaxN * kChunk, *accC = accB + kMaxN * kChunk;  // [n][item][lane]
     float *redB = accC + kMaxN * kChunk, *redC = redB + kWarps * kChunk;  // [warp][item][lane]
     float *spar = redC + kWarps * kChunk;  // [warp][A, entering state, leaving adjoint][n]
+    float *stg = spar + kWarps * 3 * kMaxN;  // staged rows of the current 8 channels
     const ChunkCtx c = chunk_ctx(p);
     load_bc_tiles(p, c, Bs, Cs, sizeof(IO) == 2);
     for (int i = threadIdx.x; i < kMaxN * kChunk; i += kThreads) accB[i] = accC[i] = 0.0f;
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = p.N;
-    IO *dxp = static_cast<IO *>(p.dx);
-    IO *ddp = static_cast<IO *>(p.ddelta);
     float *par = spar + warp * 3 * kMaxN;
 
     for (int dbase = c.d0; dbase < c.d1; dbase += kWarps) {
@@ -321,8 +431,11 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
             par[kMaxN + lane] = dok ? p.carH[cidx] : 0.0f;
             par[2 * kMaxN + lane] = dok ? p.carM[cidx] : 0.0f;
         }
+        if (dbase > c.d0) __syncthreads();  // the previous block's rows are stored
+        stage_rows<IO>(p, c, dbase, stg);
+        __syncthreads();
         float dl[kItems], x[kItems], gy[kItems], v[kItems], xdl[kItems];
-        load_items<IO>(p, c, d, dok, lane, dl, x, gy, v);
+        read_items(p, c, stg, dok, warp, lane, dl, x, gy, v);
         // S = sum_n lam B (dx = dl S, ddelta gets x S), G = sum_n lam dA h_prev A
         float S[kItems], G[kItems];
 #pragma unroll
@@ -385,24 +498,22 @@ __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
             }
             __syncthreads();
         }
-        if (dok) {
-            const float Dd = p.Dskip ? p.Dskip[d] : 0.0f;
-            float sdx = 0.0f;
+        // dx and ddelta into this lane's staged x and delta slots (only its
+        // own slots: no other thread reads them before the barrier below)
+        const float Dd = dok && p.Dskip ? p.Dskip[d] : 0.0f;
+        float sdx = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kItems; ++i) {
-                const long long t = c.t0 + lane * kItems + i;
-                sdx = fmaf(gy[i], x[i], sdx);
-                if (t < p.L) {
-                    const long long gidx = (c.b * p.L + t) * p.D + d;
-                    const float gdl = fmaf(x[i], S[i], G[i]);
-                    st_io(dxp, gidx, fmaf(gy[i], Dd, dl[i] * S[i]));
-                    st_io(ddp, gidx, p.softplus ? gdl * softplus_grad(v[i]) : gdl);
-                }
-            }
-            sdx = warp_sum(sdx);
-            if (lane == 0) p.partD[(c.b * p.K + c.k) * p.D + d] = sdx;
+        for (int i = 0; i < kItems; ++i) {
+            const int sl = stage_slot(i, lane);
+            const float gdl = fmaf(x[i], S[i], G[i]);
+            sdx = fmaf(gy[i], x[i], sdx);
+            stg[(1 * kWarps + warp) * kChunk + sl] = fmaf(gy[i], Dd, dl[i] * S[i]);
+            stg[(0 * kWarps + warp) * kChunk + sl] = p.softplus ? gdl * softplus_grad(v[i]) : gdl;
         }
-        __syncwarp();  // par is rewritten for the next channel
+        sdx = warp_sum(sdx);
+        if (dok && lane == 0) p.partD[(c.b * p.K + c.k) * p.D + d] = sdx;
+        __syncthreads();  // the block's dx, ddelta are staged
+        store_rows<IO>(p, c, dbase, stg);
     }
     // this channel range's dB, dC over the chunk
     const int r = (int)(blockIdx.x % p.SD);
@@ -527,15 +638,23 @@ ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cu
     p.SD = pl.SD;
     p.Dr = pl.Dr;
     p.softplus = a.softplus;
+    {
+        const uintptr_t es = a.io_bf16 ? 2 : 4;
+        const uintptr_t ptrs = reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.delta) |
+                               reinterpret_cast<uintptr_t>(a.dy) | reinterpret_cast<uintptr_t>(a.dx) |
+                               reinterpret_cast<uintptr_t>(a.ddelta);
+        p.vec_rows = (ptrs & 15u) == 0 && ((uintptr_t)a.D * es) % 16 == 0;
+    }
     char *ws = static_cast<char *>(workspace);
     float **sec[9] = {&p.aggP, &p.aggH, &p.aggM, &p.carH, &p.carM, &p.partA, &p.partD, &p.partB, &p.partC};
     for (int i = 0; i < 9; ++i) *sec[i] = reinterpret_cast<float *>(ws + pl.off[i]);
     const long long grid = a.B * pl.K * pl.SD;
     if (grid > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
-    if (a.io_bf16)
-        bwd_aggregate_kernel<__nv_bfloat16><<<(unsigned)grid, kThreads, 0, stream>>>(p);
-    else
-        bwd_aggregate_kernel<float><<<(unsigned)grid, kThreads, 0, stream>>>(p);
+    auto agg = a.io_bf16 ? bwd_aggregate_kernel<__nv_bfloat16> : bwd_aggregate_kernel<float>;
+    if (cudaFuncSetAttribute(agg, cudaFuncAttributeMaxDynamicSharedMemorySize, kAggSmem) !=
+        cudaSuccess)
+        return SS_ERR_CUDA;
+    agg<<<(unsigned)grid, kThreads, kAggSmem, stream>>>(p);
     const long long chains = a.B * a.D * a.N;
     bwd_carry_kernel<<<(unsigned)((chains + 255) / 256), 256, 0, stream>>>(p);
     auto grad = a.io_bf16 ? bwd_grad_kernel<__nv_bfloat16> : bwd_grad_kernel<float>;

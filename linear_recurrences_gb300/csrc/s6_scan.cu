@@ -42,6 +42,7 @@
 #include <cstdio>
 #include <cstdlib>
 
+#include "f32x2.cuh"
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
@@ -84,39 +85,6 @@ struct S6Params {
     const float *h0;      // (B, D, N) state before t = 0, or null (zeros); forward only
     float *h_last;        // (B, D, N) receives the state after t = L - 1, or null
 };
-
-// ------------------------------------------------------------------ f32x2
-typedef unsigned long long u64;
-__device__ __forceinline__ u64 f2(float lo, float hi) {
-    u64 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float f2lo(u64 v) {
-    float lo;
-    asm("mov.b64 {%0, _}, %1;" : "=f"(lo) : "l"(v));
-    return lo;
-}
-__device__ __forceinline__ float f2hi(u64 v) {
-    float hi;
-    asm("mov.b64 {_, %0}, %1;" : "=f"(hi) : "l"(v));
-    return hi;
-}
-__device__ __forceinline__ u64 f2mul(u64 a, u64 b) {
-    u64 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ u64 f2add(u64 a, u64 b) {
-    u64 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ u64 f2fma(u64 a, u64 b, u64 c) {
-    u64 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
 
 // ------------------------------------------------------------------ io helpers
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -259,20 +227,6 @@ __device__ __forceinline__ void wait_stage(const S6Params &p, WarpCtx &w, int sl
 enum { OUT_Y = 0,        // store y in the storage type
        OUT_HALF = 1,     // forward half of a bidirectional output: fp32 to yf
        OUT_SUM = 2 };    // reverse half: add the fp32 forward half, store y
-
-// 2^(delta * A2) for a pair of states in one PTX block, so both MUFU results
-// land in the two halves of one 64-bit register.
-__device__ __forceinline__ u64 f2_exp2_scaled(u64 dd, u64 a2) {
-    u64 r;
-    asm("{\n .reg .b64 t;\n .reg .f32 lo, hi;\n"
-        " mul.rn.f32x2 t, %1, %2;\n"
-        " mov.b64 {lo, hi}, t;\n"
-        " ex2.approx.ftz.f32 lo, lo;\n"
-        " ex2.approx.ftz.f32 hi, hi;\n"
-        " mov.b64 %0, {lo, hi};\n}"
-        : "=l"(r) : "l"(dd), "l"(a2));
-    return r;
-}
 
 // One timestep of this lane's chains. xv, dv: x and delta of (t, d); brow,
 // crow: Bt and Ct rows of t as fp32; yp: this lane's output element.
