@@ -31,6 +31,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 
 #include "ss_common.cuh"
 #include "ss_internal.h"
@@ -577,15 +578,44 @@ int sm_count() {
     return sms;
 }
 
+int smem_per_sm() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        v <= 0) {
+        cudaGetLastError();
+        return 233472;
+    }
+    return v;
+}
+
 BwdPlan bwd_plan(int64_t B, int64_t L, int64_t D, int64_t N) {
     BwdPlan pl{};
     pl.K = (int)((L + kChunk - 1) / kChunk);
-    // enough CTAs for about four per SM, splitting the channels into ranges
-    const long long target = (long long)sm_count() * 4;
+    // Channel ranges per (b, chunk): the gradient launch (the longest) fits
+    // 2 CTAs per SM (128 registers x 256 threads, and its shared memory), so
+    // pick the split that minimises waves x (channels per CTA + 16, the
+    // per-CTA tile loads and range sums in channel-equivalents): a last wave
+    // that only a few CTAs occupy costs as much as a full one.
     const long long groups = (D + kWarps - 1) / kWarps;
-    long long SD = (target + B * pl.K - 1) / std::max<long long>(B * pl.K, 1);
-    SD = std::max<long long>(1, std::min<long long>(SD, groups));
-    pl.Dr = (int)(((groups + SD - 1) / SD) * kWarps);
+    const long long per_sm =
+        std::max<long long>(1, std::min<long long>(2, smem_per_sm() / (kGradSmem + 1024)));
+    const long long slots = (long long)sm_count() * per_sm;
+    long long best_cost = -1, best_Dr = groups * kWarps;
+    for (long long sd = 1; sd <= std::min<long long>(groups, 64); ++sd) {
+        const long long Dr = (groups + sd - 1) / sd * kWarps;
+        const long long ctas = B * pl.K * ((D + Dr - 1) / Dr);
+        const long long cost = (ctas + slots - 1) / slots * (Dr + 16);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_Dr = Dr;
+        }
+    }
+    if (const char *e = std::getenv("SS_BWD_SD")) {  // tuning override: channel ranges
+        const long long sd = std::atoll(e);
+        if (sd >= 1 && sd <= groups) best_Dr = (groups + sd - 1) / sd * kWarps;
+    }
+    pl.Dr = (int)best_Dr;
     pl.SD = (int)((D + pl.Dr - 1) / pl.Dr);
     const size_t bkdn = (size_t)B * pl.K * D * N * sizeof(float);
     const size_t sizes[9] = {bkdn, bkdn, bkdn, bkdn, bkdn, bkdn,
