@@ -33,6 +33,7 @@
 #include <cstdint>
 #include <cstdlib>
 
+#include "f32x2.cuh"
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
@@ -44,6 +45,8 @@ constexpr int kChunk = 32 * kItems;     // steps per chunk
 constexpr int kWarps = 8;               // channels in flight per CTA
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxN = 16;
+constexpr int kMaxP = kMaxN / 2;                // state pairs (f32x2)
+constexpr u64 kOne2 = 0x3f8000003f800000ull;   // {1.0f, 1.0f}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
@@ -130,28 +133,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
     return v;
 }
-// Composition of all 32 lanes' maps in lane order (lane 0 first); lane 0
-// holds the result.
-__device__ __forceinline__ Map warp_total_fwd(Map m, int lane) {
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float a = __shfl_down_sync(kFull, m.a, off);
-        const float b = __shfl_down_sync(kFull, m.b, off);
-        if (lane + off < 32) m = then(m, {a, b});
-    }
-    return m;
-}
-// Composition in reverse lane order (lane 31 first); lane 0 holds it.
-__device__ __forceinline__ Map warp_total_rev(Map m, int lane) {
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float a = __shfl_down_sync(kFull, m.a, off);
-        const float b = __shfl_down_sync(kFull, m.b, off);
-        if (lane + off < 32) m = then({a, b}, m);
-    }
-    return m;
-}
-
 // One CTA: chunk k of batch b, channel range r. Shared Bt / Ct tiles of the
 // chunk laid out [n][item][lane], so lane reads are conflict-free.
 struct ChunkCtx {
@@ -321,51 +302,127 @@ __device__ __forceinline__ void read_items(const BwdParams &p, const ChunkCtx &c
     }
 }
 
-// ---- launch 1: per (b, chunk, d, n) the product of dA, the forward end
-// state from zero, and the adjoint entering the chunk from zero.
-constexpr int kAggSmem = (2 * kMaxN * kChunk + kWarps * kMaxN + kStageFloats) * (int)sizeof(float);
+// ---- launch 1: per (b, chunk, d, n) the product of dA over the chunk, the
+// forward end state from zero, and the adjoint entering the chunk from zero,
+// mu_in = sum_t (dA_t0 ... dA_t) dy_t C_t (the adjoint recursion mu_t =
+// dA_t (dy_t C_t + mu_t+1) unrolled from mu = 0 after the chunk). Lane =
+// channel with all 16 states as 8 f32x2 pairs in registers, as in the
+// forward kernel, sweeping steps in order (no warp scans). A CTA is 32
+// consecutive channels of one chunk; its kAggWarps warps take consecutive
+// quarters of the chunk's steps, and warp 0 folds the quarters' (P, H, M)
+// in time order: (P, H, M) then (P', H', M') = (P P', P' H + H', M + P M').
+constexpr int kAggWarps = 4;
+constexpr int kAggSteps = kChunk / kAggWarps;  // steps per warp
+constexpr int kAggSmem =
+    (2 * kChunk * kMaxN + 3 * (kAggWarps - 1) * 32 * kMaxN) * (int)sizeof(float);  // 38 KB
 
 template <typename IO>
-__global__ void __launch_bounds__(kThreads) bwd_aggregate_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(32 * kAggWarps, 4) bwd_aggregate_kernel(const BwdParams p) {
     extern __shared__ __align__(16) float smem[];  // kAggSmem bytes
-    float *Bs = smem, *Cs = Bs + kMaxN * kChunk;
-    float *sA = Cs + kMaxN * kChunk;  // [warp][n]
-    float *stg = sA + kWarps * kMaxN;
-    const ChunkCtx c = chunk_ctx(p);
-    load_bc_tiles(p, c, Bs, Cs, sizeof(IO) == 2);
+    float *sB = smem, *sC = smem + kChunk * kMaxN;  // [step][16], zeros past N and L
+    u64 *fold = reinterpret_cast<u64 *>(sC + kChunk * kMaxN);  // [warp-1][P, H, M][pair][lane]
+    const long long groups = (p.D + 31) / 32;
+    const long long bk = blockIdx.x / groups;
+    const long long b = bk / p.K;
+    const int k = (int)(bk % p.K);
+    const long long t0 = (long long)k * kChunk;
+    const int steps = (int)min((long long)kChunk, p.L - t0);
+    const int N = p.N;
+    for (int idx = threadIdx.x; idx < kChunk * kMaxN; idx += 32 * kAggWarps) {
+        const int tl = idx / kMaxN, n = idx - tl * kMaxN;
+        float bv = 0.0f, cv = 0.0f;
+        if (tl < steps && n < N) {
+            const long long g = (b * p.L + t0 + tl) * N + n;
+            bv = ld_io(static_cast<const IO *>(p.Bt), g);
+            cv = ld_io(static_cast<const IO *>(p.Ct), g);
+        }
+        sB[idx] = bv;
+        sC[idx] = cv;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int dbase = c.d0; dbase < c.d1; dbase += kWarps) {
-        const int d = dbase + warp;
-        const bool dok = d < c.d1;  // warp-uniform
-        if (dbase > c.d0) __syncthreads();  // the previous block's items are read
-        stage_rows<IO>(p, c, dbase, stg);
-        if (dok && lane < p.N) sA[warp * kMaxN + lane] = p.A[(long long)d * p.N + lane] * kLog2e;
-        __syncthreads();  // rows staged (and the first time the B, C tiles)
-        if (!dok) continue;
-        float dl[kItems], x[kItems], gy[kItems], v[kItems];
-        read_items(p, c, stg, true, warp, lane, dl, x, gy, v);
+    const long long d = (blockIdx.x % groups) * 32 + lane;
+    const bool dok = d < p.D;
+    u64 A2[kMaxP], P[kMaxP], H[kMaxP], M[kMaxP];
 #pragma unroll
-        for (int i = 0; i < kItems; ++i) x[i] *= dl[i];  // x now holds dl * x
-        for (int n = 0; n < p.N; ++n) {
-            const float A2 = sA[warp * kMaxN + n];
-            float dA[kItems];
-            Map f = {1.0f, 0.0f};
+    for (int q = 0; q < kMaxP; ++q) {
+        const int n0 = 2 * q;
+        const float a0 = dok && n0 < N ? p.A[d * N + n0] * kLog2e : 0.0f;
+        const float a1 = dok && n0 + 1 < N ? p.A[d * N + n0 + 1] * kLog2e : 0.0f;
+        A2[q] = f2(a0, a1);  // a missing state: dA = 1, B = C = 0, so it stays (1, 0, 0)
+        P[q] = kOne2;
+        H[q] = M[q] = 0ull;
+    }
+    __syncthreads();  // the Bt, Ct rows are in place
+    const IO *xp = static_cast<const IO *>(p.x);
+    const IO *dp = static_cast<const IO *>(p.delta);
+    const IO *yp = static_cast<const IO *>(p.dy);
+    const int s0 = warp * kAggSteps, s1 = min(steps, s0 + kAggSteps);
+#pragma unroll 4
+    for (int tl = s0; tl < s1; ++tl) {
+        float v = 0.0f, x = 0.0f, gy = 0.0f;
+        if (dok) {
+            const long long g = (b * p.L + t0 + tl) * p.D + d;
+            v = ld_io(dp, g);
+            x = ld_io(xp, g);
+            gy = ld_io(yp, g);
+        }
+        const float dl = dok ? (p.softplus ? softplus_fwd(v) : v) : 0.0f;
+        const float u = dl * x;
+        const u64 dd = f2(dl, dl), uu = f2(u, u), gg = f2(gy, gy);
+        const float4 *Bq = reinterpret_cast<const float4 *>(sB + tl * kMaxN);
+        const float4 *Cq = reinterpret_cast<const float4 *>(sC + tl * kMaxN);
 #pragma unroll
-            for (int i = 0; i < kItems; ++i) {
-                dA[i] = ex2_approx(dl[i] * A2);
-                f = {f.a * dA[i], fmaf(dA[i], f.b, x[i] * Bs[n * kChunk + i * 32 + lane])};
+        for (int h4 = 0; h4 < kMaxN / 4; ++h4) {
+            const float4 b4 = Bq[h4], c4 = Cq[h4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int q = 2 * h4 + e;
+                const u64 Bp = e ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
+                const u64 Cp = e ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
+                const u64 dA = f2_exp2_scaled(dd, A2[q]);
+                H[q] = f2fma(dA, H[q], f2mul(uu, Bp));
+                P[q] = f2mul(P[q], dA);
+                M[q] = f2fma(P[q], f2mul(gg, Cp), M[q]);
             }
-            float m = 0.0f;  // adjoint: mu_in -> f.a mu_in + m
+        }
+    }
+    if (warp > 0) {
+        u64 *f = fold + (warp - 1) * 3 * kMaxP * 32;
 #pragma unroll
-            for (int i = kItems - 1; i >= 0; --i) m = dA[i] * (gy[i] * Cs[n * kChunk + i * 32 + lane] + m);
-            const Map r = warp_total_rev({f.a, m}, lane);
-            f = warp_total_fwd(f, lane);
-            if (lane == 0) {
-                const long long idx = ((c.b * p.K + c.k) * p.D + d) * p.N + n;
-                p.aggP[idx] = f.a;
-                p.aggH[idx] = f.b;
-                p.aggM[idx] = r.b;
-            }
+        for (int q = 0; q < kMaxP; ++q) {
+            f[(0 * kMaxP + q) * 32 + lane] = P[q];
+            f[(1 * kMaxP + q) * 32 + lane] = H[q];
+            f[(2 * kMaxP + q) * 32 + lane] = M[q];
+        }
+    }
+    __syncthreads();
+    if (warp > 0 || !dok) return;
+#pragma unroll
+    for (int w = 1; w < kAggWarps; ++w) {
+        const u64 *f = fold + (w - 1) * 3 * kMaxP * 32;
+#pragma unroll
+        for (int q = 0; q < kMaxP; ++q) {
+            const u64 P2 = f[(0 * kMaxP + q) * 32 + lane];
+            const u64 H2 = f[(1 * kMaxP + q) * 32 + lane];
+            const u64 M2 = f[(2 * kMaxP + q) * 32 + lane];
+            M[q] = f2fma(P[q], M2, M[q]);
+            H[q] = f2fma(P2, H[q], H2);
+            P[q] = f2mul(P[q], P2);
+        }
+    }
+    const long long base = ((b * p.K + k) * p.D + d) * N;
+#pragma unroll
+    for (int q = 0; q < kMaxP; ++q) {
+        const int n0 = 2 * q;
+        if (n0 < N) {
+            p.aggP[base + n0] = f2lo(P[q]);
+            p.aggH[base + n0] = f2lo(H[q]);
+            p.aggM[base + n0] = f2lo(M[q]);
+        }
+        if (n0 + 1 < N) {
+            p.aggP[base + n0 + 1] = f2hi(P[q]);
+            p.aggH[base + n0 + 1] = f2hi(H[q]);
+            p.aggM[base + n0 + 1] = f2hi(M[q]);
         }
     }
 }
@@ -680,11 +737,13 @@ ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cu
     for (int i = 0; i < 9; ++i) *sec[i] = reinterpret_cast<float *>(ws + pl.off[i]);
     const long long grid = a.B * pl.K * pl.SD;
     if (grid > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
+    const long long agg_grid = a.B * pl.K * ((a.D + 31) / 32);
+    if (agg_grid > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
     auto agg = a.io_bf16 ? bwd_aggregate_kernel<__nv_bfloat16> : bwd_aggregate_kernel<float>;
     if (cudaFuncSetAttribute(agg, cudaFuncAttributeMaxDynamicSharedMemorySize, kAggSmem) !=
         cudaSuccess)
         return SS_ERR_CUDA;
-    agg<<<(unsigned)grid, kThreads, kAggSmem, stream>>>(p);
+    agg<<<(unsigned)agg_grid, 32 * kAggWarps, kAggSmem, stream>>>(p);
     const long long chains = a.B * a.D * a.N;
     bwd_carry_kernel<<<(unsigned)((chains + 255) / 256), 256, 0, stream>>>(p);
     auto grad = a.io_bf16 ? bwd_grad_kernel<__nv_bfloat16> : bwd_grad_kernel<float>;
