@@ -264,9 +264,11 @@ ss_status ss_selective_scan_fwd_state(const void *x, const void *delta,
  * proj_delta, [D, D + N) proj_B, [D + N, D + 2N) proj_C. b_delta: (D,) fp32.
  * A: (D, N) fp32 (already negative); Dskip: (D,) fp32 or NULL. proj_B and
  * proj_C carry no bias (the pages give one for proj_delta only).
- * The projections are dense GEMMs run by cuBLASLt with fp32 accumulation
- * into the workspace (projection outputs in io_dtype); the bias and softplus
- * are applied inside the scan. The workspace
+ * The three projections are one dense GEMM, x times W_proj transposed, run
+ * by cuBLASLt with fp32 accumulation into one (B*L) x (D + 2N) workspace
+ * buffer of io_dtype (a row: pre-activation, B_t, C_t of one step); the
+ * scan reads the three blocks at that row stride and applies the bias and
+ * softplus itself. The workspace
  * (ss_selective_scan_layer_workspace_bytes) holds the projections, the
  * GEMM scratch and the scan's workspace (first, so ss_get_device_status
  * reads the scan's error word from it); zero it once before first use, as

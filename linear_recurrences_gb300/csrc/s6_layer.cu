@@ -2,11 +2,13 @@
 //
 // "POPCORNBENCH FW-GLM-5-1 l2_p30", the model's parameters and forward pass:
 // delta = softplus(proj_delta(x)) with a bias, B_t = proj_B(x), C_t =
-// proj_C(x), then the S6 recurrence. The projections are plain dense GEMMs
-// (x is (B*L) x D, the weights D x D and D x N) and run as cuBLASLt matmuls
-// (bf16 or fp32 inputs, fp32 accumulation) into the workspace; the delta
-// bias and softplus are fused into the scan, which reads the projections
-// straight from there.
+// proj_C(x), then the S6 recurrence. The three projections are one dense
+// GEMM: x ((B*L) x D) times the stacked weights W_proj ((D + 2N) x D)
+// transposed, a single cuBLASLt matmul (bf16 or fp32 inputs, fp32
+// accumulation) into one (B*L) x (D + 2N) workspace buffer whose row holds
+// the pre-activation, B_t and C_t of one step; the scan reads the three
+// column blocks in place at that row stride, with the delta bias and
+// softplus fused in.
 #include <cublasLt.h>
 
 #include <algorithm>
@@ -78,7 +80,7 @@ ss_status gemm_xwT(const void *x, const void *W, void *out, int64_t M, int64_t K
 }
 
 struct LayerPlan {
-    size_t pre, bt, ct, lt, scan, total;  // section offsets, then total bytes
+    size_t proj, lt, scan, total;  // section offsets, then total bytes
 };
 
 LayerPlan layer_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16) {
@@ -88,10 +90,8 @@ LayerPlan layer_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16) {
     // the scan's section comes first, so the workspace starts with its
     // header (error word) even when the scan needs no further workspace
     pl.scan = 0;
-    pl.pre = std::max<size_t>(kWsHeaderBytes, align256(s6_workspace_bytes(B, L, D, N, io_bf16, 0)));
-    pl.bt = pl.pre + align256(M * D * es);
-    pl.ct = pl.bt + align256(M * N * es);
-    pl.lt = pl.ct + align256(M * N * es);
+    pl.proj = std::max<size_t>(kWsHeaderBytes, align256(s6_workspace_bytes(B, L, D, N, io_bf16, 0)));
+    pl.lt = pl.proj + align256(M * (size_t)(D + 2 * N) * es);
     pl.total = pl.lt + kLtWorkspace;
     return pl;
 }
@@ -113,21 +113,19 @@ ss_status layer_fwd_launch(const void *x, const void *W_proj, const float *b_del
         return SS_ERR_WORKSPACE;
     char *ws = static_cast<char *>(workspace);
     const size_t es = io_bf16 ? 2 : 4;
-    const char *Wc = static_cast<const char *>(W_proj);
     const int64_t M = B * L;
-    // rows [0, D) of W_proj: proj_delta; [D, D + N): proj_B; [D + N, D + 2N): proj_C
-    ss_status st = gemm_xwT(x, Wc, ws + pl.pre, M, D, D, io_bf16, ws + pl.lt, stream);
-    if (st == SS_OK)
-        st = gemm_xwT(x, Wc + (size_t)D * D * es, ws + pl.bt, M, D, N, io_bf16, ws + pl.lt, stream);
-    if (st == SS_OK)
-        st = gemm_xwT(x, Wc + (size_t)(D + N) * D * es, ws + pl.ct, M, D, N, io_bf16, ws + pl.lt,
-                      stream);
+    // rows [0, D) of W_proj: proj_delta; [D, D + N): proj_B; [D + N, D + 2N):
+    // proj_C, so output row m is (pre-activation, B_t, C_t) of step m
+    const ss_status st =
+        gemm_xwT(x, W_proj, ws + pl.proj, M, D, D + 2 * N, io_bf16, ws + pl.lt, stream);
     if (st != SS_OK) return st;
     S6Args a;
     a.x = x;
-    a.delta = ws + pl.pre;
-    a.Bt = ws + pl.bt;
-    a.Ct = ws + pl.ct;
+    a.delta = ws + pl.proj;
+    a.Bt = ws + pl.proj + (size_t)D * es;
+    a.Ct = ws + pl.proj + (size_t)(D + N) * es;
+    a.ld_delta = D + 2 * N;
+    a.ld_bc = D + 2 * N;
     a.A = A;
     a.Dskip = Dskip;
     a.y = y;
@@ -141,7 +139,7 @@ ss_status layer_fwd_launch(const void *x, const void *W_proj, const float *b_del
     a.io_bf16 = io_bf16;
     a.softplus = 1;
     a.bidir = 0;
-    return s6_launch(a, ws + pl.scan, pl.pre - pl.scan, stream, timeout_ns, skip_unit);
+    return s6_launch(a, ws + pl.scan, pl.proj - pl.scan, stream, timeout_ns, skip_unit);
 }
 
 }  // namespace ss

@@ -70,6 +70,7 @@ struct S6Params {
     void *y;
     float *yscratch;   // bidirectional bf16: fp32 forward outputs (B, L, D)
     long long L, D;
+    long long ldd, ldbc;  // row strides (elements) of delta and of Bt, Ct
     int N;
     int dtiles;        // ceil(D / 32)
     int K;             // chunks per sequence
@@ -199,14 +200,14 @@ __device__ __forceinline__ void issue_stage(const S6Params &p, WarpCtx &w, int s
         // unaligned shapes: plain loads, synchronous
         if (w.half == 0) {
             for (int r = 0; r < nrows; ++r) {
-                const long long gi = (row0 + r) * p.D + w.d;
-                xs[r * CPW + w.ch] = w.dvalid ? xg[gi] : IO(0.0f);
-                ds[r * CPW + w.ch] = w.dvalid ? dg[gi] : IO(0.0f);
+                xs[r * CPW + w.ch] = w.dvalid ? xg[(row0 + r) * p.D + w.d] : IO(0.0f);
+                ds[r * CPW + w.ch] = w.dvalid ? dg[(row0 + r) * p.ldd + w.d] : IO(0.0f);
             }
         }
         for (int i = w.lane; i < nrows * N; i += 32) {
-            bs[i] = bg[row0 * N + i];
-            if (MODE == MODE_OUT) cs[i] = cg[row0 * N + i];
+            const long long gi = (row0 + i / N) * p.ldbc + i % N;
+            bs[i] = bg[gi];
+            if (MODE == MODE_OUT) cs[i] = cg[gi];
         }
         __syncwarp();
     }
@@ -887,14 +888,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Row-major 2D map over `rows` rows of `inner` elements, box = box_inner x box_rows.
-bool encode_2d(CUtensorMap *m, const void *base, bool bf16, uint64_t inner, uint64_t rows,
-               uint32_t box_inner, uint32_t box_rows) {
+// Row-major 2D map over `rows` rows of `inner` elements, `ld` elements apart,
+// box = box_inner x box_rows.
+bool encode_2d(CUtensorMap *m, const void *base, bool bf16, uint64_t inner, uint64_t ld,
+               uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const uint64_t es = bf16 ? 2 : 4;
     cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * es};
+    cuuint64_t strides[1] = {ld * es};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
@@ -976,19 +978,22 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
     prm.WT = pl.WT;
     prm.Tsub = pl.Tsub;
     const size_t es = a.io_bf16 ? 2 : 4;
+    prm.ldd = a.ld_delta > 0 ? a.ld_delta : a.D;
+    prm.ldbc = a.ld_bc > 0 ? a.ld_bc : a.N;
     const uintptr_t al = reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.delta) |
                          reinterpret_cast<uintptr_t>(a.Bt) | reinterpret_cast<uintptr_t>(a.Ct);
-    prm.bulk = ((a.D * es) % 16 == 0) && ((a.N * es) % 16 == 0) && (al % 16 == 0) &&
-               (a.B * a.L < (1LL << 31)) && (a.D < (1LL << 31));
+    prm.bulk = ((a.D * es) % 16 == 0) && ((a.N * es) % 16 == 0) && ((prm.ldd * es) % 16 == 0) &&
+               ((prm.ldbc * es) % 16 == 0) && (al % 16 == 0) && (a.B * a.L < (1LL << 31)) &&
+               (a.D < (1LL << 31));
     if (prm.bulk) {
         const bool bf = a.io_bf16 != 0;
         const uint64_t rows = (uint64_t)(a.B * a.L);
         const uint32_t cpw = 32u / (uint32_t)pl.LPC;
         const uint32_t kTS = bf ? Ring<__nv_bfloat16>::kTS : Ring<float>::kTS;
-        prm.bulk = encode_2d(&prm.tm_x, a.x, bf, a.D, rows, cpw, kTS) &&
-                   encode_2d(&prm.tm_d, a.delta, bf, a.D, rows, cpw, kTS) &&
-                   encode_2d(&prm.tm_b, a.Bt, bf, a.N, rows, (uint32_t)a.N, kTS) &&
-                   encode_2d(&prm.tm_c, a.Ct, bf, a.N, rows, (uint32_t)a.N, kTS);
+        prm.bulk = encode_2d(&prm.tm_x, a.x, bf, a.D, a.D, rows, cpw, kTS) &&
+                   encode_2d(&prm.tm_d, a.delta, bf, a.D, prm.ldd, rows, cpw, kTS) &&
+                   encode_2d(&prm.tm_b, a.Bt, bf, a.N, prm.ldbc, rows, (uint32_t)a.N, kTS) &&
+                   encode_2d(&prm.tm_c, a.Ct, bf, a.N, prm.ldbc, rows, (uint32_t)a.N, kTS);
     }
     prm.timeout_ns = timeout_ns;
     prm.skip_unit = skip_unit;

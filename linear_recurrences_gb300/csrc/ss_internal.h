@@ -31,6 +31,8 @@ struct S6Args {
     const float *delta_bias = nullptr;  // (D,) added to delta before softplus, or null
     const float *h0;  // (B, D, N) initial state or null (zeros); forward only
     float *h_last;    // (B, D, N) final state or null; forward only
+    int64_t ld_delta = 0;  // row stride (elements) of delta; 0: D (dense)
+    int64_t ld_bc = 0;     // row stride (elements) of Bt and Ct; 0: N (dense)
     int64_t B, L, D, N;
     int io_bf16;
     int softplus;
