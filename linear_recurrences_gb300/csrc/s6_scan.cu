@@ -817,22 +817,30 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     if (bidir) Tsub = std::max<long long>(Tsub, (L + (long long)WT * sms - 1) / ((long long)WT * sms));
     // whole waves: a CTA count just above a multiple of what fits at once
     // leaves most SMs idle in the last wave. For plans of more than one
-    // wave, among sub-chunk lengths down to half of the above, take the one
-    // minimising waves x (steps per warp + 16, the per-chunk fold and
+    // wave, among sub-chunk lengths from half of the above (up to one and a
+    // half times it for bidirectional plans, whose residency bound already
+    // lengthens them and whose working set stays well inside L2), take the
+    // one minimising waves x (steps per warp + 16, the per-chunk fold and
     // look-back in steps); 4-warp CTAs fit 3 per SM by their launch bounds,
     // fewer if shared memory runs out first.
-    if (!bidir && WT == kMaxWT && (long long)WT * Tsub < L) {
+    if (WT == kMaxWT && (long long)WT * Tsub < L) {
         const size_t ring = io_bf16 ? Ring<__nv_bfloat16>::kWarp : Ring<float>::kWarp;
         const size_t smem = 128 + (size_t)WT * (ring + kMaxStages * sizeof(uint64_t)) +
-                            (size_t)(WT * 2 + 1) * 32 * pl.NG * sizeof(float);
+                            (size_t)(WT * (bidir ? 3 : 2) + (bidir ? 2 : 1)) * 32 * pl.NG *
+                                sizeof(float);
         const long long per_sm =
             std::max<long long>(1, std::min<long long>(3, device_smem_per_sm() / (long long)(smem + 1024)));
         const long long slots = sms * per_sm;
         const long long K0 = (L + (long long)WT * Tsub - 1) / ((long long)WT * Tsub);
+        long long lo = std::max<long long>(kTS, Tsub / 2 / kTS * kTS);
+        if (bidir) {  // keep the residency bound
+            const long long rb = (L + (long long)WT * sms - 1) / ((long long)WT * sms);
+            lo = std::max<long long>(lo, (rb + kTS - 1) / kTS * kTS);
+        }
+        const long long hi = bidir ? (Tsub + Tsub / 2) / kTS * kTS : Tsub;
         long long best_cost = -1, best_T = Tsub;
         // (within one wave there is nothing to fill: keep the plan)
-        for (long long T = Tsub; pl.seqs * K0 > slots && T >= std::max<long long>(kTS, Tsub / 2);
-             T -= kTS) {
+        for (long long T = hi; pl.seqs * K0 > slots && T >= lo; T -= kTS) {
             const long long Kc = (L + (long long)WT * T - 1) / ((long long)WT * T);
             const long long waves = (pl.seqs * Kc + slots - 1) / slots;
             const long long cost = waves * (T + 16);
