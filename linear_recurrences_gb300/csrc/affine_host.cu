@@ -35,18 +35,36 @@ struct Pipe {
 std::mutex g_mu;
 Pipe g_pipes[kMaxDevices];
 
+// Releases whatever a failed make_pipe created, leaving p as it started.
+void drop_pipe(Pipe &p) {
+    cudaEvent_t *evs[] = {&p.start, &p.done};
+    for (cudaEvent_t *e : evs)
+        if (*e) cudaEventDestroy(*e);
+    for (int s = 0; s < kSlots; ++s) {
+        if (p.loaded[s]) cudaEventDestroy(p.loaded[s]);
+        if (p.scanned[s]) cudaEventDestroy(p.scanned[s]);
+        if (p.drained[s]) cudaEventDestroy(p.drained[s]);
+    }
+    if (p.up) cudaStreamDestroy(p.up);
+    if (p.down) cudaStreamDestroy(p.down);
+    cudaGetLastError();
+    p = Pipe{};
+}
+
 bool make_pipe(Pipe &p) {
     const unsigned ev = cudaEventDisableTiming;
-    if (cudaStreamCreateWithFlags(&p.up, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&p.down, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p.start, ev) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p.done, ev) != cudaSuccess)
+    bool ok = cudaStreamCreateWithFlags(&p.up, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p.down, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.start, ev) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p.done, ev) == cudaSuccess;
+    for (int s = 0; ok && s < kSlots; ++s)
+        ok = cudaEventCreateWithFlags(&p.loaded[s], ev) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p.scanned[s], ev) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p.drained[s], ev) == cudaSuccess;
+    if (!ok) {
+        drop_pipe(p);
         return false;
-    for (int s = 0; s < kSlots; ++s)
-        if (cudaEventCreateWithFlags(&p.loaded[s], ev) != cudaSuccess ||
-            cudaEventCreateWithFlags(&p.scanned[s], ev) != cudaSuccess ||
-            cudaEventCreateWithFlags(&p.drained[s], ev) != cudaSuccess)
-            return false;
+    }
     p.ready = true;
     return true;
 }
