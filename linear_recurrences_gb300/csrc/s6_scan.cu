@@ -53,6 +53,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxWT = 4;       // warps per CTA along time (hard limit)
 constexpr int kDefaultWT = 4;   // default: small CTAs so several fit per SM
+// CTAs of kMaxWT warps that the launch bounds guarantee per SM (registers)
+template <bool BIDIR> constexpr int kMinCtas = 3;
 constexpr int kMaxWindows = 4;  // look-back holds up to 128 predecessor chunks
 constexpr int kMaxStages = 3;   // ring slots (and mbarriers) per warp, at most
 constexpr unsigned kFull = 0xffffffffu;
@@ -530,7 +532,7 @@ __device__ __forceinline__ float initial_state(const S6Params &p, const WarpCtx 
 
 // ------------------------------------------------------------------ kernel
 template <int NG, int LPC, typename IO, bool SP, bool BIDIR>
-__global__ void __launch_bounds__(kMaxWT * 32, 3)
+__global__ void __launch_bounds__(kMaxWT * 32, kMinCtas<BIDIR>)
 s6_kernel(const __grid_constant__ S6Params p) {
     constexpr int CPW = 32 / LPC;  // channels per warp
     constexpr int NSUB = BIDIR ? 3 : 2;  // sub-aggregate fields: P, H (, Hr)
@@ -821,15 +823,16 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     // half times it for bidirectional plans, whose residency bound already
     // lengthens them and whose working set stays well inside L2), take the
     // one minimising waves x (steps per warp + 16, the per-chunk fold and
-    // look-back in steps); 4-warp CTAs fit 3 per SM by their launch bounds,
-    // fewer if shared memory runs out first.
+    // look-back in steps); 4-warp CTAs fit kMinCtas per SM by their launch
+    // bounds, fewer if shared memory runs out first.
     if (WT == kMaxWT && (long long)WT * Tsub < L) {
         const size_t ring = io_bf16 ? Ring<__nv_bfloat16>::kWarp : Ring<float>::kWarp;
         const size_t smem = 128 + (size_t)WT * (ring + kMaxStages * sizeof(uint64_t)) +
                             (size_t)(WT * (bidir ? 3 : 2) + (bidir ? 2 : 1)) * 32 * pl.NG *
                                 sizeof(float);
         const long long per_sm =
-            std::max<long long>(1, std::min<long long>(3, device_smem_per_sm() / (long long)(smem + 1024)));
+            std::max<long long>(1, std::min<long long>(bidir ? kMinCtas<true> : kMinCtas<false>,
+                                                       device_smem_per_sm() / (long long)(smem + 1024)));
         const long long slots = sms * per_sm;
         const long long K0 = (L + (long long)WT * Tsub - 1) / ((long long)WT * Tsub);
         long long lo = std::max<long long>(kTS, Tsub / 2 / kTS * kTS);
