@@ -624,28 +624,6 @@ struct BwdPlan {
     size_t total;
 };
 
-int sm_count() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms <= 0) {
-        cudaGetLastError();
-        return 152;
-    }
-    return sms;
-}
-
-int smem_per_sm() {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        v <= 0) {
-        cudaGetLastError();
-        return 233472;
-    }
-    return v;
-}
-
 BwdPlan bwd_plan(int64_t B, int64_t L, int64_t D, int64_t N) {
     BwdPlan pl{};
     pl.K = (int)((L + kChunk - 1) / kChunk);
@@ -656,8 +634,8 @@ BwdPlan bwd_plan(int64_t B, int64_t L, int64_t D, int64_t N) {
     // that only a few CTAs occupy costs as much as a full one.
     const long long groups = (D + kWarps - 1) / kWarps;
     const long long per_sm =
-        std::max<long long>(1, std::min<long long>(2, smem_per_sm() / (kGradSmem + 1024)));
-    const long long slots = (long long)sm_count() * per_sm;
+        std::max<long long>(1, std::min<long long>(2, device_smem_per_sm() / (kGradSmem + 1024)));
+    const long long slots = (long long)device_sm_count() * per_sm;
     long long best_cost = -1, best_Dr = groups * kWarps;
     for (long long sd = 1; sd <= std::min<long long>(groups, 64); ++sd) {
         const long long Dr = (groups + sd - 1) / sd * kWarps;
@@ -751,7 +729,7 @@ ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cu
         cudaSuccess)
         return SS_ERR_CUDA;
     grad<<<(unsigned)grid, kThreads, kGradSmem, stream>>>(p);
-    bwd_final_kernel<<<sm_count() * 8, 256, 0, stream>>>(p);
+    bwd_final_kernel<<<device_sm_count() * 8, 256, 0, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

@@ -763,27 +763,6 @@ struct Plan {
     size_t smem;
 };
 
-int device_sm_count() {
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
-        cudaGetLastError();
-        return 152;
-    }
-    return sms;
-}
-
-int device_smem_per_sm() {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        v <= 0) {
-        cudaGetLastError();
-        return 233472;
-    }
-    return v;
-}
-
 Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir) {
     Plan pl{};
     const long long sms = device_sm_count();

@@ -9,6 +9,28 @@
 
 namespace ss {
 
+// SMs and shared memory per SM of the current device (planning inputs; the
+// GB300's values if the query fails, e.g. in a process without a GPU).
+inline int device_sm_count() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return v;
+}
+inline int device_smem_per_sm() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        v <= 0) {
+        cudaGetLastError();
+        return 233472;
+    }
+    return v;
+}
+
 size_t affine_workspace_bytes(int64_t n);
 // log_step_tiles: scan each tile with the log-step (Hillis-Steele) algorithm
 // instead of the work-efficient register scan (comparison variant).
