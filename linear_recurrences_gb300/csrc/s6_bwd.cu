@@ -12,12 +12,14 @@
 //   dh0 = mu_0,  and ddelta = ddl * sigmoid(v) under softplus.
 // (h_t - u_t = dA_t h_{t-1}, so no earlier state is needed.)
 //
-// Layout: time-parallel. A warp owns one channel of a 256-step chunk, lane l
-// the 8 consecutive steps 8l .. 8l+7, and loops over the states n; h and mu
-// for one n are warp scans (ordered shuffles) over the lanes' local affine
-// maps, so no per-(t, n) tensor is stored. Four launches:
+// Layout of the gradients: time-parallel. A warp owns one channel of a
+// 256-step chunk, lane l the 8 consecutive steps 8l .. 8l+7, and loops over
+// the states n; h and mu for one n are warp scans (ordered shuffles) over
+// the lanes' local affine maps, so no per-(t, n) tensor is stored. Four
+// launches:
 //   1. chunk aggregates (prod dA, forward end state from 0, adjoint entry
-//      from 0) per (b, chunk, d, n);
+//      from 0) per (b, chunk, d, n), in the forward kernel's layout instead
+//      (lane = channel, its 16 states in registers, steps in order);
 //   2. carries: one thread per (b, d, n) walks the chunks forward (state
 //      entering each chunk, from h0) and backward (adjoint leaving each
 //      chunk, from dh_last; dh0 at the end);
