@@ -157,3 +157,48 @@ def test_product_path_never_touches_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f"{f} mentions the oracle"
+
+
+def _s6_chunks(L, B, Lq, D, N, io, bidir):
+    """Chunks per sequence of the forward plan, read back from the workspace
+    size (header, 16-byte flags and NF fields of 32 x 16 floats per chunk)."""
+    wb = L.ss_selective_scan_workspace_bytes(B, Lq, D, N, io, bidir)
+    seqs, nf = B * ((D + 31) // 32), 5 if bidir else 3
+    scratch = B * Lq * D * 4 if (bidir and io == ss.SS_BF16) else 0
+    for K in range(1, 1024):
+        flags = (seqs * K * 16 + 255) // 256 * 256
+        if wb == 256 + flags + seqs * K * nf * 32 * 16 * 4 + scratch:
+            return K
+    raise AssertionError(f"workspace size {wb} matches no chunk count")
+
+
+def test_forward_plans_fill_whole_waves(L):
+    """The planner's sub-chunk choice for the three S6 workloads on 152 SMs
+    (the values it falls back to without a GPU): 7 chunks of 4 x 80 steps
+    for fp32 (896 CTAs, 1.96 waves of 456), 8 of 4 x 128 for bf16, 27 of
+    4 x 152 for the bidirectional workload (1296 CTAs, 2.84 waves)."""
+    assert _s6_chunks(L, 16, 2048, 256, 16, ss.SS_F32, 0) == 7
+    assert _s6_chunks(L, 8, 4096, 1536, 16, ss.SS_BF16, 0) == 8
+    assert _s6_chunks(L, 2, 16384, 768, 16, ss.SS_F32, 1) == 27
+    # within one wave the plan is left alone
+    assert _s6_chunks(L, 1, 1000, 96, 16, ss.SS_F32, 0) == 8
+
+
+def _bwd_ranges(L, B, Lq, D, N):
+    """Channel ranges of the backward plan, from its workspace size: six
+    (B, K, D, N) sections, one (B, K, D), two (ranges, B, L, N)."""
+    K = (Lq + 255) // 256
+    al = lambda v: (v + 255) // 256 * 256
+    fixed = 6 * al(B * K * D * N * 4) + al(B * K * D * 4)
+    rest = L.ss_selective_scan_bwd_workspace_bytes(B, Lq, D, N) - fixed
+    for sd in range(1, 1025):
+        if rest == 2 * al(sd * B * Lq * N * 4):
+            return sd
+    raise AssertionError("workspace size matches no channel split")
+
+
+def test_backward_plans_fill_whole_waves(L):
+    """Channel ranges per (b, chunk) minimising waves x (channels + 16) at 2
+    gradient CTAs per SM on 152 SMs: 2 for the fp32 workload, 7 for bf16."""
+    assert _bwd_ranges(L, 16, 2048, 256, 16) == 2
+    assert _bwd_ranges(L, 8, 4096, 1536, 16) == 7
