@@ -1,8 +1,9 @@
 /*
  * ss_testing.h - test hook of libss.so (not for production use).
  *
- * There is no counterpart on the pages: this exists so the test suite can
- * check the library's failure path without faulting or hanging a GPU.
+ * There is no counterpart on the pages: these exist so the test suite can
+ * check the library's failure path without faulting or hanging a GPU, and
+ * run each kernel variant on shapes the planner would give to another.
  */
 #ifndef SS_TESTING_H
 #define SS_TESTING_H
@@ -23,6 +24,31 @@ extern "C" {
  * to one launch and is then cleared. unit < 0 clears a pending request.
  */
 void ss_testing_skip_publish_once(int64_t unit);
+
+/*
+ * Forces the plan the S6 forward, state and bidirectional calls (and their
+ * workspace-size queries) use from now on, so tests can run every code path
+ * on any shape. kind 0 restores the planner's own choice. kind 1: the
+ * chunked kernel with `a` warps per CTA along time and `b` timesteps per
+ * warp (a == b == 0: the planner's values) and `c` lanes per channel (2 or
+ * 4; 0 or 1: one); kind 2: the time-parallel single pass with `a` channels
+ * per warp, `b` steps per lane and `c` warps per CTA (built variants: a in
+ * {2, 4}, b in {7, 9}; forward calls only, else the planner's choice
+ * applies). A workspace sized under one setting is only valid under that
+ * setting; calls made while another thread changes it may take either.
+ */
+void ss_testing_s6_plan(int kind, int a, int b, int c);
+
+/*
+ * Describes the plan an S6 call of this shape would use under the current
+ * setting: returns 1 for the time-parallel single pass (out = channels per
+ * warp, steps per lane, warps per CTA, blocks per sequence, CTAs, steps per
+ * block), 0 for the chunked kernel (out = lanes per channel, warps per CTA,
+ * timesteps per warp, chunks per sequence, CTAs, states per lane), -1 for an
+ * invalid shape. out: six host int64 values.
+ */
+int ss_testing_s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,
+                                int bidir, int64_t *out);
 
 #ifdef __cplusplus
 }

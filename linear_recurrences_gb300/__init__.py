@@ -26,6 +26,7 @@ __all__ = [
     "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
+    "ss_testing_s6_plan", "ss_testing_s6_describe_plan",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
     "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
     "ss_selective_scan_layer_fwd", "ss_selective_scan_layer_workspace_bytes",
@@ -41,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
+    "ss_testing_s6_plan", "ss_testing_s6_describe_plan",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_selective_scan_fwd_state",
     "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
     "ss_selective_scan_layer_workspace_bytes", "ss_selective_scan_layer_fwd",
@@ -52,6 +54,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _DEFAULT_LIB = os.path.join(_PKG, "_build", "libss.so")
 _lock = threading.Lock()
 _lib = None
+_plan_generation = 0  # bumped by ss_testing_s6_plan: cached S6 workspaces are keyed on it
 
 
 class SSError(RuntimeError):
@@ -101,6 +104,11 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_set_spin_timeout_ns.restype = ci
     L.ss_testing_skip_publish_once.argtypes = [i64]
     L.ss_testing_skip_publish_once.restype = None
+    L.ss_testing_s6_plan.argtypes = [ci, ci, ci, ci]
+    L.ss_testing_s6_plan.restype = None
+    L.ss_testing_s6_describe_plan.argtypes = [i64, i64, i64, i64, ci, ci,
+                                              ctypes.POINTER(ctypes.c_int64)]
+    L.ss_testing_s6_describe_plan.restype = ci
     L.ss_probe_mufu_ex2.argtypes = [vp, ci, ci, vp]
     L.ss_probe_mufu_ex2.restype = ci
     L.ss_affine_scan_noalloc.argtypes = [vp, vp, vp, i64, vp]
@@ -148,6 +156,28 @@ def ss_testing_skip_publish_once(unit: int) -> None:
     """Test hook (include/ss_testing.h): the next launch lets work unit `unit`
     skip publishing its look-back descriptors, so waits on it time out."""
     lib().ss_testing_skip_publish_once(int(unit))
+
+
+def ss_testing_s6_plan(kind: int = 0, a: int = 0, b: int = 0, c: int = 0) -> None:
+    """Test hook (include/ss_testing.h): forces the S6 plan for later calls;
+    kind 0 restores the planner's choice, 1 = chunked (warps per CTA,
+    timesteps per warp, lanes per channel), 2 = time-parallel (channels per
+    warp, steps per lane, warps per CTA)."""
+    global _plan_generation
+    lib().ss_testing_s6_plan(int(kind), int(a), int(b), int(c))
+    _plan_generation += 1
+
+
+def ss_testing_s6_describe_plan(B, L, D, N, io_dtype=SS_F32, bidir=False):
+    """(kind, six parameters) of the plan an S6 call of this shape would use:
+    kind 1 = time-parallel (channels per warp, steps per lane, warps per CTA,
+    blocks per sequence, CTAs, steps per block), 0 = chunked (lanes per
+    channel, warps per CTA, timesteps per warp, chunks, CTAs, states per
+    lane)."""
+    out = (ctypes.c_int64 * 6)()
+    k = lib().ss_testing_s6_describe_plan(int(B), int(L), int(D), int(N), int(io_dtype),
+                                          int(bool(bidir)), out)
+    return k, tuple(out)
 
 
 def ss_probe_mufu_ex2(out, blocks: int, iters: int, stream=None) -> None:
@@ -368,7 +398,7 @@ def _s6(fn_name, x, delta, Bt, Ct, A, Dskip, delta_softplus, y, workspace, strea
     sh = _stream_handle(stream, x.device)
     need = ss_selective_scan_workspace_bytes(B, L, D, N, io_dtype, bidir)
     if workspace is None and need:
-        key = (fn_name, B, L, D, N, io_dtype, need, os.environ.get("SS_S6_WT_TSUB"))
+        key = (fn_name, B, L, D, N, io_dtype, need, _plan_generation)
         workspace = _cached_workspace(key, need, x.device, sh)
     wsb = workspace.numel() if workspace is not None else 0
     if state is not None:  # (h0, h_last) of the forward-with-state call
@@ -499,8 +529,7 @@ def ss_selective_scan_layer_fwd(x, W_proj, b_delta, A, Dskip=None, y=None, works
     sh = _stream_handle(stream, x.device)
     need = ss_selective_scan_layer_workspace_bytes(B, L, D, N, io_dtype)
     if workspace is None and need:
-        key = ("ss_selective_scan_layer_fwd", B, L, D, N, io_dtype, need,
-               os.environ.get("SS_S6_WT_TSUB"))
+        key = ("ss_selective_scan_layer_fwd", B, L, D, N, io_dtype, need, _plan_generation)
         workspace = _cached_workspace(key, need, x.device, sh)
     wsb = workspace.numel() if workspace is not None else 0
     st = lib().ss_selective_scan_layer_fwd(_ptr(x), _ptr(W_proj), _ptr(b_delta), _ptr(A),

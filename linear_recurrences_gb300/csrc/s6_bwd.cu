@@ -36,6 +36,7 @@
 #include <cstdlib>
 
 #include "f32x2.cuh"
+#include "s6_common.cuh"
 #include "ss_common.cuh"
 #include "ss_internal.h"
 
@@ -49,8 +50,6 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxN = 16;
 constexpr int kMaxP = kMaxN / 2;                // state pairs (f32x2)
 constexpr u64 kOne2 = 0x3f8000003f800000ull;   // {1.0f, 1.0f}
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct BwdParams {
@@ -78,15 +77,6 @@ __device__ __forceinline__ float ld_io(const __nv_bfloat16 *p, long long i) {
     return __bfloat162float(p[i]);
 }
 
-// softplus(v) = log(1 + exp(v)), v > 20 passes through; the same MUFU form,
-// with the series for small exp(v), as the forward kernels use.
-__device__ __forceinline__ float softplus_fwd(float v) {
-    const float e = ex2_approx(fminf(v, 20.0f) * kLog2e);
-    const float series = e * (1.0f - e * (0.5f - e * (1.0f / 3.0f - 0.25f * e)));
-    const float logged = lg2_approx(1.0f + e) * kLn2;
-    const float r = e < 0.015625f ? series : logged;
-    return v > 20.0f ? v : r;
-}
 // d softplus / dv = sigmoid(v); 1 above the pass-through threshold.
 __device__ __forceinline__ float softplus_grad(float v) {
     return v > 20.0f ? 1.0f : 1.0f / (1.0f + ex2_approx(-v * kLog2e));
@@ -300,7 +290,7 @@ __device__ __forceinline__ void read_items(const BwdParams &p, const ChunkCtx &c
         x[i] = stg[(1 * kWarps + warp) * kChunk + s];
         gy[i] = stg[(2 * kWarps + warp) * kChunk + s];
         const bool ok = dok && c.t0 + lane * kItems + i < p.L;  // else dA = 1: an identity step
-        dl[i] = ok ? (p.softplus ? softplus_fwd(v[i]) : v[i]) : 0.0f;
+        dl[i] = ok ? (p.softplus ? softplus_mufu(v[i]) : v[i]) : 0.0f;
     }
 }
 
@@ -368,7 +358,7 @@ __global__ void __launch_bounds__(32 * kAggWarps, 4) bwd_aggregate_kernel(const 
             x = ld_io(xp, g);
             gy = ld_io(yp, g);
         }
-        const float dl = dok ? (p.softplus ? softplus_fwd(v) : v) : 0.0f;
+        const float dl = dok ? (p.softplus ? softplus_mufu(v) : v) : 0.0f;
         const float u = dl * x;
         const u64 dd = f2(dl, dl), uu = f2(u, u), gg = f2(gy, gy);
         const float4 *Bq = reinterpret_cast<const float4 *>(sB + tl * kMaxN);

@@ -38,19 +38,20 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <cstdio>
 #include <cstdlib>
 
 #include "f32x2.cuh"
+#include "s6_common.cuh"
 #include "ss_common.cuh"
 #include "ss_internal.h"
+#include "s6_tp.h"
 
 namespace ss {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxWT = 4;       // warps per CTA along time (hard limit)
 constexpr int kDefaultWT = 4;   // default: small CTAs so several fit per SM
 // CTAs of kMaxWT warps that the launch bounds guarantee per SM (registers)
@@ -88,24 +89,6 @@ struct S6Params {
     const float *h0;      // (B, D, N) state before t = 0, or null (zeros); forward only
     float *h_last;        // (B, D, N) receives the state after t = L - 1, or null
 };
-
-// ------------------------------------------------------------------ io helpers
-__device__ __forceinline__ float to_f32(float v) { return v; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ void store_io(float *p, float v) { __stcs(p, v); }
-__device__ __forceinline__ void store_io(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
-
-// softplus(v) = log(1 + exp(v)); v > 20 returns v. exp and log on MUFU; for
-// exp(v) < 1/64 the log is replaced by its alternating series so that the
-// rounding of 1 + exp(v) does not swamp small results. Both forms are
-// computed and selected, so the step has no branch.
-__device__ __forceinline__ float softplus_mufu(float v) {
-    const float e = ex2_approx(fminf(v, 20.0f) * kLog2e);
-    const float series = e * (1.0f - e * (0.5f - e * (1.0f / 3.0f - 0.25f * e)));
-    const float logged = lg2_approx(1.0f + e) * kLn2;
-    const float r = e < 0.015625f ? series : logged;
-    return v > 20.0f ? v : r;
-}
 
 template <int NG>
 __device__ __forceinline__ float *field_ptr(const S6Params &p, int NF, long long unit, int field,
@@ -761,7 +744,22 @@ struct Plan {
     long long seqs;
     size_t flag_bytes, payload_bytes, scratch_bytes, desc_bytes, total;
     size_t smem;
+    bool tp;      // the time-parallel single pass (s6_tp.cu) runs this shape
+    TPPlan tpp;   // its launch shape; its packed B_t / C_t follow the chunked
+                  // plan's section of the workspace
+    size_t tp_offset;
 };
+
+// Plan override for tests (ss_testing_s6_plan): kind 0 = the planner's
+// choice; 1 = the chunked kernel with (WT, Tsub) = (a, b) (0, 0 = the
+// planner's) and c lanes per channel (0 or 1: one); 2 = the time-parallel
+// single pass with (G, T, W) = (a, b, c).
+std::atomic<int> g_ovr_kind{0}, g_ovr_a{0}, g_ovr_b{0}, g_ovr_c{0};
+// The time-parallel pass is built and tested but not yet taken by default:
+// measured on GB300 it does not beat the chunked kernel on the fp32 and bf16
+// forward workloads (its per-pair scan costs as many instructions as the
+// chunked kernel's second sweep).
+constexpr bool kTPByDefault = false;
 
 Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir) {
     Plan pl{};
@@ -771,8 +769,9 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     // Two lanes per channel (8 states each) doubles the warps but repeats the
     // per-timestep scalar work on both lanes; measured slower on every S6
     // shape tried, so it is only taken on request.
-    if (const char *e = std::getenv("SS_S6_LPC")) {  // tuning override: 1, 2 or 4
-        const int v = std::atoi(e);
+    const int ovr = g_ovr_kind.load();
+    if (ovr == 1) {  // test override: 2 or 4 lanes per channel
+        const int v = g_ovr_c.load();
         if ((v == 2 || v == 4) && pl.NG == 16) {
             pl.NG = 16 / v;
             pl.LPC = v;
@@ -833,9 +832,9 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
         }
         Tsub = best_T;
     }
-    if (const char *e = std::getenv("SS_S6_WT_TSUB")) {  // tuning override "WT,Tsub"
-        int wv = 0, tv = 0;
-        if (std::sscanf(e, "%d,%d", &wv, &tv) == 2 && wv >= 1 && wv <= kMaxWT && tv >= 1) {
+    if (ovr == 1) {  // test override of (warps per CTA, timesteps per warp)
+        const int wv = g_ovr_a.load(), tv = g_ovr_b.load();
+        if (wv >= 1 && wv <= kMaxWT && tv >= 1) {  // (0, 0): keep the planner's
             WT = wv;
             Tsub = tv;
         }
@@ -858,41 +857,37 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     const size_t ring = io_bf16 ? Ring<__nv_bfloat16>::kWarp : Ring<float>::kWarp;
     pl.smem = 128 + (size_t)pl.WT * (ring + kMaxStages * sizeof(uint64_t)) +
               (size_t)(pl.WT * NSUB + (bidir ? 2 : 1)) * 32 * pl.NG * sizeof(float);
-    return pl;
-}
 
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
-// (the library does not link libcuda).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *sym = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &sym, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(sym);
-        cudaGetLastError();
-    });
-    return fn;
+    // The time-parallel single pass computes each term's exp once and needs
+    // no look-back, but its parallelism is one warp per G channels: it runs
+    // forward shapes whose channels alone keep the SMs busy (tp_choose_plan).
+    pl.tp = false;
+    pl.tp_offset = 0;
+    if (!bidir && ovr != 1) {
+        TPPlan tpp{};
+        const bool ok = ovr == 2 ? tp_make_plan(B, L, D, N, io_bf16, g_ovr_a.load(),
+                                                g_ovr_b.load(), g_ovr_c.load(), &tpp)
+                                 : (kTPByDefault && tp_choose_plan(B, L, D, N, io_bf16, (int)sms, &tpp));
+        if (ok) {
+            pl.tp = true;
+            pl.tpp = tpp;
+            const size_t base = std::max<size_t>(pl.total, kWsHeaderBytes);
+            pl.tp_offset = (base + 255) / 256 * 256;
+            pl.total = pl.tp_offset + tpp.pack_bytes;
+        }
+    }
+    return pl;
 }
 
 // Row-major 2D map over `rows` rows of `inner` elements, `ld` elements apart,
 // box = box_inner x box_rows.
 bool encode_2d(CUtensorMap *m, const void *base, bool bf16, uint64_t inner, uint64_t ld,
                uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
     const uint64_t es = bf16 ? 2 : 4;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {ld * es};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const uint64_t dims[2] = {inner, rows};
+    const uint64_t strides[1] = {ld * es};
+    const uint32_t box[2] = {box_inner, box_rows};
+    return encode_tiled_map(m, base, bf16, 2, dims, strides, box);
 }
 
 template <int NG, int LPC, typename IO, bool SP, bool BIDIR>
@@ -939,6 +934,71 @@ ss_status launch_io(const S6Params &prm, const Plan &pl, bool sp, bool bidir, cu
 
 }  // namespace
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library does not link libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *sym = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &sym, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(sym);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+bool encode_tiled_map(void *map, const void *base, bool bf16, int rank, const uint64_t *dims,
+                      const uint64_t *strides, const uint32_t *box) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return enc(static_cast<CUtensorMap *>(map),
+               bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+               (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void s6_set_plan_override(int kind, int a, int b, int c) {
+    g_ovr_a.store(a);
+    g_ovr_b.store(b);
+    g_ovr_c.store(c);
+    g_ovr_kind.store(kind >= 0 && kind <= 2 ? kind : 0);
+}
+
+int s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir,
+                     int64_t *out) {
+    if (B <= 0 || L <= 0 || D <= 0 || N <= 0 || N > 16) return -1;
+    const Plan pl = make_plan(B, L, D, N, io_bf16, bidir);
+    if (pl.tp) {
+        out[0] = pl.tpp.G;
+        out[1] = pl.tpp.T;
+        out[2] = pl.tpp.W;
+        out[3] = pl.tpp.nblk;
+        out[4] = pl.tpp.ctas;
+        out[5] = pl.tpp.R;
+        return 1;
+    }
+    out[0] = pl.LPC;
+    out[1] = pl.WT;
+    out[2] = pl.Tsub;
+    out[3] = pl.K;
+    out[4] = pl.seqs * pl.K;
+    out[5] = pl.NG;
+    return 0;
+}
+
 size_t s6_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir) {
     if (B <= 0 || L <= 0 || D <= 0 || N <= 0) return 0;
     return make_plan(B, L, D, N, io_bf16, bidir).total;
@@ -951,6 +1011,17 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
         if (workspace == nullptr || ws_bytes < pl.total ||
             (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return SS_ERR_WORKSPACE;
+    }
+    if (pl.tp) {
+        // tile copies need 16-byte aligned rows and bases (else the chunked
+        // kernel below runs, with its own section of the workspace)
+        const size_t es = a.io_bf16 ? 2 : 4;
+        const int64_t ldd = a.ld_delta > 0 ? a.ld_delta : a.D;
+        const uintptr_t al = reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.delta) |
+                             reinterpret_cast<uintptr_t>(a.y);
+        if ((a.D * es) % 16 == 0 && (ldd * es) % 16 == 0 && al % 16 == 0) {
+            return tp_launch(a, pl.tpp, workspace, pl.tp_offset, stream, timeout_ns);
+        }
     }
     S6Params prm{};
     prm.x = a.x;

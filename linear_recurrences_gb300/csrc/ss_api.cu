@@ -271,6 +271,14 @@ ss_status ss_get_device_status(void *workspace, void *stream) {
 
 void ss_testing_skip_publish_once(int64_t unit) { g_skip_unit.store(unit < 0 ? -1 : unit); }
 
+void ss_testing_s6_plan(int kind, int a, int b, int c) { ss::s6_set_plan_override(kind, a, b, c); }
+
+int ss_testing_s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,
+                                int bidir, int64_t *out) {
+    if (!out || (io_dtype != SS_F32 && io_dtype != SS_BF16)) return -1;
+    return ss::s6_describe_plan(B, L, D, N, io_dtype == SS_BF16, bidir != 0, out);
+}
+
 ss_status ss_set_spin_timeout_ns(uint64_t ns) {
     if (ns == 0) return SS_ERR_INVALID;
     g_timeout_ns.store(ns);

@@ -184,6 +184,53 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity
     return true;
 }
 
+// 3D tile copy global -> shared through a tensor map, completing on `bar`.
+// Coordinates (x, y, z) innermost first; boxes reaching past the tensor's
+// extent arrive zero-filled. dst 128-byte aligned.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z),
+          "r"(smem_addr(bar)) : "memory");
+}
+// 3D tile copy shared -> global through a tensor map (bulk async-group);
+// elements of the box outside the tensor's extent are not written. Writers
+// of the tile must have executed fence_proxy_async_smem() and synchronised
+// with the issuing thread first.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most N bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until at most N bulk groups of this thread are still in flight.
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------------ dependent launches
+// Lets the next kernel of the stream, if launched as a programmatic dependent,
+// start its prologue while this one runs.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have finished and their memory
+// is visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ cp.async (LDGSTS)
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src, unsigned src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"

@@ -31,6 +31,15 @@ inline int device_smem_per_sm() {
     return v;
 }
 
+// Encodes a tiled TMA tensor map (cuTensorMapEncodeTiled through the
+// runtime's driver entry point) into `map` (a 128-byte CUtensorMap): `rank`
+// dimensions innermost first, dims[i] elements each, strides[i] bytes
+// between consecutive indices of dimension i + 1, box[i] elements per copy,
+// fp32 or bf16 elements, no swizzle, zero fill outside the extent. false if
+// the entry point is missing or the driver rejects the layout.
+bool encode_tiled_map(void *map, const void *base, bool bf16, int rank, const uint64_t *dims,
+                      const uint64_t *strides, const uint32_t *box);
+
 size_t affine_workspace_bytes(int64_t n);
 // log_step_tiles: scan each tile with the log-step (Hillis-Steele) algorithm
 // instead of the work-efficient register scan (comparison variant).
@@ -65,6 +74,11 @@ struct S6Args {
 unsigned long long spin_timeout_ns();
 
 size_t s6_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir);
+// Test hooks behind ss_testing_s6_plan / ss_testing_s6_describe_plan.
+void s6_set_plan_override(int kind, int a, int b, int c);
+int s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir,
+                     int64_t *out);
+
 
 struct S6BwdArgs {
     const void *x, *delta, *Bt, *Ct, *dy;

@@ -159,29 +159,65 @@ def test_product_path_never_touches_the_oracle():
                 assert "oracle" not in text.lower(), f"{f} mentions the oracle"
 
 
-def _s6_chunks(L, B, Lq, D, N, io, bidir):
-    """Chunks per sequence of the forward plan, read back from the workspace
-    size (header, 16-byte flags and NF fields of 32 x 16 floats per chunk)."""
-    wb = L.ss_selective_scan_workspace_bytes(B, Lq, D, N, io, bidir)
-    seqs, nf = B * ((D + 31) // 32), 5 if bidir else 3
-    scratch = B * Lq * D * 4 if (bidir and io == ss.SS_BF16) else 0
-    for K in range(1, 1024):
-        flags = (seqs * K * 16 + 255) // 256 * 256
-        if wb == 256 + flags + seqs * K * nf * 32 * 16 * 4 + scratch:
-            return K
-    raise AssertionError(f"workspace size {wb} matches no chunk count")
+def _chunked_plan(B, Lq, D, N, io, bidir):
+    """(chunks per sequence, warps per CTA, timesteps per warp) the chunked
+    kernel's planner takes for a shape (the time-parallel pass set aside)."""
+    ss.ss_testing_s6_plan(1, 0, 0, 1)
+    try:
+        kind, p = ss.ss_testing_s6_describe_plan(B, Lq, D, N, io, bidir)
+    finally:
+        ss.ss_testing_s6_plan(0)
+    assert kind == 0
+    return p[3], p[1], p[2]
 
 
 def test_forward_plans_fill_whole_waves(L):
-    """The planner's sub-chunk choice for the three S6 workloads on 152 SMs
-    (the values it falls back to without a GPU): 7 chunks of 4 x 80 steps
-    for fp32 (896 CTAs, 1.96 waves of 456), 8 of 4 x 128 for bf16, 27 of
-    4 x 152 for the bidirectional workload (1296 CTAs, 2.84 waves)."""
-    assert _s6_chunks(L, 16, 2048, 256, 16, ss.SS_F32, 0) == 7
-    assert _s6_chunks(L, 8, 4096, 1536, 16, ss.SS_BF16, 0) == 8
-    assert _s6_chunks(L, 2, 16384, 768, 16, ss.SS_F32, 1) == 27
+    """The chunked planner's sub-chunk choice for the three S6 workloads on
+    152 SMs (the values it falls back to without a GPU): 7 chunks of 4 x 80
+    steps for fp32 (896 CTAs, 1.96 waves of 456), 8 of 4 x 128 for bf16, 27
+    of 4 x 152 for the bidirectional workload (1296 CTAs, 2.84 waves)."""
+    assert _chunked_plan(16, 2048, 256, 16, ss.SS_F32, 0) == (7, 4, 80)
+    assert _chunked_plan(8, 4096, 1536, 16, ss.SS_BF16, 0) == (8, 4, 128)
+    assert _chunked_plan(2, 16384, 768, 16, ss.SS_F32, 1) == (27, 4, 152)
     # within one wave the plan is left alone
-    assert _s6_chunks(L, 1, 1000, 96, 16, ss.SS_F32, 0) == 8
+    assert _chunked_plan(1, 1000, 96, 16, ss.SS_F32, 0)[0] == 8
+
+
+def test_planner_paths(L):
+    """Bidirectional shapes and forward shapes with few channels take the
+    chunked kernel; the test override forces the time-parallel pass on
+    forward shapes only."""
+    assert ss.ss_testing_s6_describe_plan(2, 16384, 768, 16, ss.SS_F32, 1)[0] == 0
+    assert ss.ss_testing_s6_describe_plan(1, 5000, 64, 16, ss.SS_F32, 0)[0] == 0
+    ss.ss_testing_s6_plan(2, 4, 9, 2)
+    try:
+        k, p = ss.ss_testing_s6_describe_plan(1, 5000, 64, 16, ss.SS_F32, 0)
+        assert k == 1 and p[:3] == (4, 9, 2)
+        assert ss.ss_testing_s6_describe_plan(1, 5000, 64, 16, ss.SS_F32, 1)[0] == 0
+    finally:
+        ss.ss_testing_s6_plan(0)
+    assert ss.ss_testing_s6_describe_plan(1, 10, 8, 17, ss.SS_F32, 0)[0] == -1
+
+
+def test_time_parallel_workspace_size(L):
+    """Forward workspace of a time-parallel plan: the chunked plan's section
+    (for inputs whose rows turn out unaligned), then the packed B_t / C_t:
+    per sequence and block, ceil(N / 8) slots of 2 matrices x 4 state pairs
+    x 16 slices x 5 float4 (80-byte slice rows)."""
+    B, Lq, D, N = 16, 2048, 256, 16
+    nblk = (Lq + 143) // 144
+    pack = B * nblk * 2 * (2 * 4 * 16 * 80)
+    ss.ss_testing_s6_plan(1, 0, 0, 1)
+    try:
+        chunked = L.ss_selective_scan_workspace_bytes(B, Lq, D, N, ss.SS_F32, 0)
+    finally:
+        ss.ss_testing_s6_plan(0)
+    ss.ss_testing_s6_plan(2, 2, 9, 4)
+    try:
+        total = L.ss_selective_scan_workspace_bytes(B, Lq, D, N, ss.SS_F32, 0)
+    finally:
+        ss.ss_testing_s6_plan(0)
+    assert total == (chunked + 255) // 256 * 256 + pack
 
 
 def _bwd_ranges(L, B, Lq, D, N):

@@ -25,17 +25,13 @@ def ss():
 
 
 @pytest.fixture
-def plan_override():
-    """Sets the S6 tuning override (warps per CTA, timesteps per warp) for one test."""
-    old = os.environ.get("SS_S6_WT_TSUB")
-
-    def set_(wt, tsub):
-        os.environ["SS_S6_WT_TSUB"] = f"{wt},{tsub}"
+def plan_override(ss):
+    """Forces the chunked kernel with (warps per CTA, timesteps per warp, lanes
+    per channel) for one test, through the library's test hook."""
+    def set_(wt, tsub, lpc=1):
+        ss.ss_testing_s6_plan(1, wt, tsub, lpc)
     yield set_
-    if old is None:
-        os.environ.pop("SS_S6_WT_TSUB", None)
-    else:
-        os.environ["SS_S6_WT_TSUB"] = old
+    ss.ss_testing_s6_plan(0)
 
 
 def gpu_run(ss, torch, inp, softplus, bidir):
@@ -218,30 +214,47 @@ def test_timeout_is_reported_not_hung(torch, ss, plan_override, bidir):
     assert rel_err(to_host_f64(out), oracle_run(inp, False, bidir)) <= TOL["f32"]
 
 
-@pytest.fixture
-def lane_layout():
-    """Forces one, two or four lanes per channel (SS_S6_LPC) for one test."""
-    old = os.environ.get("SS_S6_LPC")
-
-    def set_(v):
-        os.environ["SS_S6_LPC"] = str(v)
-    yield set_
-    if old is None:
-        os.environ.pop("SS_S6_LPC", None)
-    else:
-        os.environ["SS_S6_LPC"] = old
-
-
 @pytest.mark.parametrize("lpc", [1, 2, 4])
 @pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
 @pytest.mark.parametrize("io,softplus", [("f32", False), ("bf16", True)])
-def test_both_lane_layouts(torch, ss, lane_layout, plan_override, lpc, bidir, io, softplus):
-    """16 states per lane, or 8 / 4 states on each of two / four lanes per
-    channel; the register path (one warp over all of L) and a chunked plan."""
-    lane_layout(lpc)
-    for wt_tsub in (None, (2, 24)):
-        if wt_tsub:
-            plan_override(*wt_tsub)
+def test_both_lane_layouts(torch, ss, plan_override, lpc, bidir, io, softplus):
+    """The chunked kernel with 16 states per lane, or 8 / 4 states on each of
+    two / four lanes per channel: under its planner's own split of L and a
+    forced split of 2 warps x 24 steps."""
+    for wt_tsub in ((0, 0), (2, 24)):
+        plan_override(*wt_tsub, lpc)
         inp = small(2, 333, 70, 16, io=io, softplus=softplus, seed=7 + lpc)
         y = gpu_run(ss, torch, inp, softplus, bidir)
         assert rel_err(y, oracle_run(inp, softplus, bidir)) <= TOL[io]
+
+
+@pytest.mark.parametrize("bidir", [False, True], ids=["fwd", "bidir"])
+@pytest.mark.parametrize("io,softplus", [("f32", False), ("bf16", True)])
+def test_register_path_long_sequence(torch, ss, plan_override, bidir, io, softplus):
+    """The chunked kernel's register path: one warp per 32 channels runs all
+    of a 3000-step sequence (one chunk, one warp per CTA), forced by plan."""
+    L = 3000
+    plan_override(1, L)
+    B, D, N = 2, 70, 16
+    kind, prm = ss.ss_testing_s6_describe_plan(B, L, D, N, ss.SS_BF16 if io == "bf16" else ss.SS_F32,
+                                               bidir)
+    assert kind == 0 and prm[1] == 1 and prm[3] == 1  # one warp per CTA, one chunk
+    inp = small(B, L, D, N, io=io, softplus=softplus, seed=31)
+    y = gpu_run(ss, torch, inp, softplus, bidir)
+    assert rel_err(y, oracle_run(inp, softplus, bidir)) <= TOL[io]
+
+
+def test_register_path_chosen_for_many_channels(torch, ss):
+    """A bidirectional shape with B*D large enough to fill the chip with one
+    warp per 32 channels takes the register path by itself (L = 1024, 80,000
+    channels); sampled channels against the oracle."""
+    B, L, D, N = 1, 1024, 80000, 16
+    kind, prm = ss.ss_testing_s6_describe_plan(B, L, D, N, ss.SS_F32, True)
+    assert kind == 0 and prm[1] == 1 and prm[3] == 1
+    inp = workloads.s6_inputs(B, L, D, N, io="f32", delta="loguniform", dskip="normal", seed=41)
+    y = gpu_run(ss, torch, inp, False, True)
+    chans = _sample_channels(B, D, 200, seed=2)
+    ref = oracle.s6_channels(inp.x_f32, inp.delta_f32, inp.Bt_f32, inp.Ct_f32, inp.A, inp.Dskip,
+                             chans, softplus=False, bidir=True, threads=THREADS)
+    got = np.stack([y[c // D, :, c % D] for c in chans])
+    assert rel_err(got, ref) <= TOL["f32"]

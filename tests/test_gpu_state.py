@@ -27,19 +27,19 @@ def ss():
 
 
 @pytest.fixture
-def plan_override():
-    old = os.environ.get("SS_S6_WT_TSUB")
-
-    def set_(wt, tsub):
+def plan_override(ss):
+    """Forces a plan for one test through the library's test hook: (wt, tsub)
+    for the chunked kernel, ("tp", G, T, W) for the time-parallel pass, None
+    for the planner's own choice."""
+    def set_(wt, tsub=0, *rest):
         if wt is None:
-            os.environ.pop("SS_S6_WT_TSUB", None)
+            ss.ss_testing_s6_plan(0)
+        elif wt == "tp":
+            ss.ss_testing_s6_plan(2, tsub, *rest)
         else:
-            os.environ["SS_S6_WT_TSUB"] = f"{wt},{tsub}"
+            ss.ss_testing_s6_plan(1, wt, tsub, 1)
     yield set_
-    if old is None:
-        os.environ.pop("SS_S6_WT_TSUB", None)
-    else:
-        os.environ["SS_S6_WT_TSUB"] = old
+    ss.ss_testing_s6_plan(0)
 
 
 def inputs(B, L, D, N, io="f32", softplus=False, seed=0):
@@ -79,10 +79,13 @@ def oracle_state(inp, h0, softplus, t0=0, t1=None):
 
 SHAPES = [(1, 1, 1, 1), (2, 5, 3, 4), (1, 40, 32, 16), (2, 100, 33, 16), (3, 257, 40, 3),
           (2, 600, 64, 16)]
-PLANS = [None, (1, 8), (2, 16), (4, 5), (2, 1024)]  # default, chunked, unsplit multi-warp
+# default, chunked, unsplit multi-warp, time-parallel (channels/warp, steps/lane, warps/CTA)
+PLANS = [None, (1, 8), (2, 16), (4, 5), (2, 1024), ("tp", 2, 9, 4), ("tp", 4, 9, 2),
+         ("tp", 8, 9, 2)]
 
 
-@pytest.mark.parametrize("plan", PLANS, ids=lambda p: "default" if p is None else f"{p[0]}x{p[1]}")
+@pytest.mark.parametrize("plan", PLANS,
+                         ids=lambda p: "default" if p is None else "x".join(map(str, p)))
 @pytest.mark.parametrize("io,softplus", [("f32", False), ("bf16", True)])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_state_parity(torch, ss, plan_override, shape, io, softplus, plan):
@@ -114,7 +117,7 @@ def test_streamed_in_pieces(torch, ss, plan_override, io, softplus):
     cuts = [0, 1, 433, 900]
     ys, h = [], h0
     for i, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
-        plan_override(*[(None, None), (1, 8), (4, 32)][i])
+        plan_override(*[(None, None), (1, 8), ("tp", 4, 9, 2)][i])
         y, h = gpu_state(ss, torch, inp, h, softplus, a, b)
         ys.append(y)
     ry, rhl = oracle_state(inp, h0.astype(np.float64), softplus)
