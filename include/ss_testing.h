@@ -33,15 +33,19 @@ void ss_testing_skip_publish_once(int64_t unit);
  * warp (a == b == 0: the planner's values) and `c` lanes per channel (2 or
  * 4; 0 or 1: one); kind 2: the time-parallel single pass with `a` channels
  * per warp, `b` steps per lane and `c` warps per CTA (built variants: a in
- * {2, 4}, b in {7, 9}; forward calls only, else the planner's choice
- * applies). A workspace sized under one setting is only valid under that
+ * {2, 4, 8}, b in {7, 9}); kind 3: the wavefront single pass with `a` steps
+ * per warp slice and `b` slices (warps) per CTA (built: (9, 4), (11, 4),
+ * (13, 4), (9, 2), (13, 2)). Kinds 2 and 3 apply to forward calls only (else the
+ * planner's choice applies). A workspace sized under one setting is only valid under that
  * setting; calls made while another thread changes it may take either.
  */
 void ss_testing_s6_plan(int kind, int a, int b, int c);
 
 /*
  * Describes the plan an S6 call of this shape would use under the current
- * setting: returns 1 for the time-parallel single pass (out = channels per
+ * setting: returns 2 for the wavefront single pass (out = steps per slice,
+ * slices per CTA, channels per CTA, blocks per sequence, CTAs, steps per
+ * block), 1 for the time-parallel single pass (out = channels per
  * warp, steps per lane, warps per CTA, blocks per sequence, CTAs, steps per
  * block), 0 for the chunked kernel (out = lanes per channel, warps per CTA,
  * timesteps per warp, chunks per sequence, CTAs, states per lane), -1 for an

@@ -162,7 +162,8 @@ def ss_testing_s6_plan(kind: int = 0, a: int = 0, b: int = 0, c: int = 0) -> Non
     """Test hook (include/ss_testing.h): forces the S6 plan for later calls;
     kind 0 restores the planner's choice, 1 = chunked (warps per CTA,
     timesteps per warp, lanes per channel), 2 = time-parallel (channels per
-    warp, steps per lane, warps per CTA)."""
+    warp, steps per lane, warps per CTA), 3 = wavefront (steps per slice,
+    slices per CTA)."""
     global _plan_generation
     lib().ss_testing_s6_plan(int(kind), int(a), int(b), int(c))
     _plan_generation += 1
@@ -170,7 +171,8 @@ def ss_testing_s6_plan(kind: int = 0, a: int = 0, b: int = 0, c: int = 0) -> Non
 
 def ss_testing_s6_describe_plan(B, L, D, N, io_dtype=SS_F32, bidir=False):
     """(kind, six parameters) of the plan an S6 call of this shape would use:
-    kind 1 = time-parallel (channels per warp, steps per lane, warps per CTA,
+    kind 2 = wavefront (steps per slice, slices, channels per CTA, blocks per
+    sequence, CTAs, steps per block), 1 = time-parallel (channels per warp, steps per lane, warps per CTA,
     blocks per sequence, CTAs, steps per block), 0 = chunked (lanes per
     channel, warps per CTA, timesteps per warp, chunks, CTAs, states per
     lane)."""

@@ -48,6 +48,7 @@
 #include "ss_common.cuh"
 #include "ss_internal.h"
 #include "s6_tp.h"
+#include "s6_ws.h"
 
 namespace ss {
 namespace {
@@ -748,12 +749,15 @@ struct Plan {
     TPPlan tpp;   // its launch shape; its packed B_t / C_t follow the chunked
                   // plan's section of the workspace
     size_t tp_offset;
+    bool ws;      // the wavefront single pass (s6_ws.cu) runs this shape
+    WSPlan wsp;   // its launch shape (it needs the workspace header only)
 };
 
 // Plan override for tests (ss_testing_s6_plan): kind 0 = the planner's
 // choice; 1 = the chunked kernel with (WT, Tsub) = (a, b) (0, 0 = the
 // planner's) and c lanes per channel (0 or 1: one); 2 = the time-parallel
-// single pass with (G, T, W) = (a, b, c).
+// single pass with (G, T, W) = (a, b, c); 3 = the wavefront single pass
+// with (T, S) = (a, b).
 std::atomic<int> g_ovr_kind{0}, g_ovr_a{0}, g_ovr_b{0}, g_ovr_c{0};
 // The time-parallel pass is built and tested but not yet taken by default:
 // measured on GB300 it does not beat the chunked kernel on the fp32 and bf16
@@ -863,6 +867,23 @@ Plan make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidi
     // forward shapes whose channels alone keep the SMs busy (tp_choose_plan).
     pl.tp = false;
     pl.tp_offset = 0;
+    pl.ws = false;
+    // The wavefront single pass computes each term's exp once, reads every
+    // input once and needs no look-back; it takes forward shapes whose
+    // channels fill the chip (ws_choose_plan), the chunked kernel the rest.
+    if (!bidir && (ovr == 3 || ovr == 0)) {
+        WSPlan wsp{};
+        const bool ok = ovr == 3 ? ws_make_plan(B, L, D, N, io_bf16, g_ovr_a.load(),
+                                                g_ovr_b.load(), &wsp)
+                                 : ws_choose_plan(B, L, D, N, io_bf16, (int)sms, &wsp);
+        if (ok) {
+            pl.ws = true;
+            pl.wsp = wsp;
+            pl.total = std::max<size_t>(pl.total, kWsHeaderBytes);
+            return pl;
+        }
+        if (ovr == 3) return pl;
+    }
     if (!bidir && ovr != 1) {
         TPPlan tpp{};
         const bool ok = ovr == 2 ? tp_make_plan(B, L, D, N, io_bf16, g_ovr_a.load(),
@@ -974,13 +995,22 @@ void s6_set_plan_override(int kind, int a, int b, int c) {
     g_ovr_a.store(a);
     g_ovr_b.store(b);
     g_ovr_c.store(c);
-    g_ovr_kind.store(kind >= 0 && kind <= 2 ? kind : 0);
+    g_ovr_kind.store(kind >= 0 && kind <= 3 ? kind : 0);
 }
 
 int s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir,
                      int64_t *out) {
     if (B <= 0 || L <= 0 || D <= 0 || N <= 0 || N > 16) return -1;
     const Plan pl = make_plan(B, L, D, N, io_bf16, bidir);
+    if (pl.ws) {
+        out[0] = pl.wsp.T;
+        out[1] = pl.wsp.S;
+        out[2] = 32;
+        out[3] = pl.wsp.nblk;
+        out[4] = pl.wsp.ctas;
+        out[5] = pl.wsp.R;
+        return 2;
+    }
     if (pl.tp) {
         out[0] = pl.tpp.G;
         out[1] = pl.tpp.T;
@@ -1011,6 +1041,18 @@ ss_status s6_launch(const S6Args &a, void *workspace, size_t ws_bytes, cudaStrea
         if (workspace == nullptr || ws_bytes < pl.total ||
             (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return SS_ERR_WORKSPACE;
+    }
+    if (pl.ws) {
+        // tile copies need 16-byte aligned rows and bases (else the chunked
+        // kernel below runs, with its own section of the workspace)
+        const size_t es = a.io_bf16 ? 2 : 4;
+        const int64_t ldd = a.ld_delta > 0 ? a.ld_delta : a.D;
+        const int64_t ldbc = a.ld_bc > 0 ? a.ld_bc : a.N;
+        const uintptr_t al = reinterpret_cast<uintptr_t>(a.x) | reinterpret_cast<uintptr_t>(a.delta) |
+                             reinterpret_cast<uintptr_t>(a.y) | reinterpret_cast<uintptr_t>(a.Bt) |
+                             reinterpret_cast<uintptr_t>(a.Ct);
+        if ((a.D * es) % 16 == 0 && (ldd * es) % 16 == 0 && (ldbc * es) % 16 == 0 && al % 16 == 0)
+            return ws_launch(a, pl.wsp, workspace, stream, timeout_ns);
     }
     if (pl.tp) {
         // tile copies need 16-byte aligned rows and bases (else the chunked
