@@ -235,7 +235,7 @@ def s6_variant(name):
     return workloads.S6[name], ""
 
 
-def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
+def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak, cpu=False):
     """One S6 workload. A name ending in "_state" runs the forward-with-state
     call from a seeded random h0, writing h_last (2 x B*D*N*4 more bytes); one
     ending in "_bwd" runs the backward pass for a seeded random dy: reads x,
@@ -271,10 +271,13 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
         # projections of the workload's shape with seeded random weights:
         # W ~ N(0, 1/D), b_delta ~ N(-4, 1) (steps like the workload's)
         g = np.random.Generator(np.random.PCG64(23))
-        W = t(g.standard_normal((w.D + 2 * w.N, w.D)).astype(np.float32) / np.sqrt(w.D))
+        W_np = (g.standard_normal((w.D + 2 * w.N, w.D)) / np.sqrt(w.D)).astype(np.float32)
+        W = t(W_np)
         if inp.io == "bf16":
             W = W.to(torch.bfloat16)
-        bd = torch.from_numpy(g.normal(-4.0, 1.0, w.D).astype(np.float32)).to(dev)
+            W_np = W.float().cpu().numpy()  # the values the GPU sees
+        bd_np = g.normal(-4.0, 1.0, w.D).astype(np.float32)
+        bd = torch.from_numpy(bd_np).to(dev)
         io_dtype = ss.SS_BF16 if w.io == "bf16" else ss.SS_F32
         lws = ss.new_workspace(
             ss.ss_selective_scan_layer_workspace_bytes(w.B, w.L, w.D, w.N, io_dtype), dev)
@@ -305,6 +308,9 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
         flush = lambda: junk.fill_(0.0)
     per, _ = time_launches(torch, call, steps, warmup, stream, flush=flush)
     ms = statistics.mean(per)
+    base = None
+    if cpu:
+        base = s6_oracle_baseline(w, variant, inp, (W_np, bd_np) if variant == "layer" else None)
     t_hbm = byts / (hbm_peak * 1e9)
     t_sfu = mufu / sfu_peak
     t_roof = max(t_hbm, t_sfu) + t_gemm
@@ -327,7 +333,59 @@ def bench_s6(torch, ss, dev, name, steps, warmup, stream, hbm_peak, sfu_peak):
             ss.ss_selective_scan_workspace_bytes(w.B, w.L, w.D, w.N,
                                                  ss.SS_BF16 if w.io == "bf16" else ss.SS_F32,
                                                  w.bidir)),
+        **({"cpu_baseline": base} if base else {}),
     }
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def s6_oracle_baseline(w, variant, inp, layer=None, elems_target=3_000_000):
+    """The float64 oracle, as it stands, on a bounded sample of one S6
+    workload: batch element 0 and its first Ls steps, Ls chosen so that the
+    sample holds about `elems_target` (b, t, d) elements (fewer for the
+    bidirectional and backward passes, which do more per element). Timed on
+    one thread and on every core this process may run on. Returns the
+    cpu_baseline object for that config's per_config entry."""
+    import numpy as np
+    import oracle
+    lib = oracle.load()
+    per_elem = {"bwd": 3, "layer": 1}.get(variant, 2 if w.bidir else 1)
+    Ls = max(1, min(w.L, elems_target // per_elem // w.D))
+    sl = lambda v: np.ascontiguousarray(v[:1, :Ls])
+    x, dl, Bt, Ct = sl(inp.x_f32), sl(inp.delta_f32), sl(inp.Bt_f32), sl(inp.Ct_f32)
+    g = np.random.Generator(np.random.PCG64(7))
+    dy = g.standard_normal((1, Ls, w.D)).astype(np.float32)
+    h0 = g.standard_normal((1, w.D, w.N))
+
+    def call(threads):
+        if variant == "bwd":
+            return oracle.s6_bwd(x, dl, Bt, Ct, inp.A, inp.Dskip, dy, softplus=w.softplus,
+                                 threads=threads, lib=lib)
+        if variant == "state":
+            return oracle.s6_fwd_state(x, dl, Bt, Ct, inp.A, inp.Dskip, h0=h0,
+                                       softplus=w.softplus, threads=threads, lib=lib)
+        if variant == "layer":
+            W, b = layer
+            return oracle.layer_fwd(x, W, b, inp.A, inp.Dskip, io=w.io, threads=threads, lib=lib)
+        f = oracle.s6_bidir if w.bidir else oracle.s6_fwd
+        return f(x, dl, Bt, Ct, inp.A, inp.Dskip, softplus=w.softplus, threads=threads, lib=lib)
+
+    cores = host_cores()
+    rates = {}
+    for threads in (1, cores):
+        t0 = time.perf_counter()
+        call(threads)
+        rates[threads] = Ls * w.D / (time.perf_counter() - t0)
+    what = {"bwd": "backward (every gradient)", "state": "forward from a state, h_last",
+            "layer": "projections (float64 numpy matmul) + scan"}.get(
+        variant, "bidirectional" if w.bidir else "forward")
+    return {"value": rates[cores], "unit": "elements/s", "cores": cores, "kind": "oracle",
+            "value_1_thread": rates[1], "host_cores": cores,
+            "sample": f"batch element 0, first {Ls} of {w.L} steps ({Ls * w.D} elements) of "
+                      f"the workload's inputs; {what}, float64, timed once on 1 thread and "
+                      f"once on {cores} threads (channels split across threads)"}
 
 
 # ---------------------------------------------------------------- arms
@@ -380,8 +438,9 @@ def cpu_baseline(budget_s: float):
             break
     dt = time.perf_counter() - t0
     return {"value": w.n * reps / dt, "unit": "elements/s", "cores": 1, "kind": "oracle",
+            "host_cores": host_cores(),
             "sample": f"full {HEADLINE} input (2**28 elements) x {reps} passes, sequential "
-                      "float64 loop, one thread"}
+                      "float64 loop, one thread (the recurrence is sequential)"}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -468,6 +527,18 @@ def run_ours(args, rank, world, local_rank):
                                    "elements_per_s": small_w.n / (sms_ * 1e-3),
                                    "gbs": 12 * small_w.n / (sms_ * 1e-3) / 1e9,
                                    "bound": "launch latency", "l2": "flushed between calls"}
+        if not args.no_cpu:
+            import oracle
+            a_s, b_s = _rest[0], _rest[1]
+            olib, reps, t0 = oracle.load(), 0, time.perf_counter()
+            while time.perf_counter() - t0 < 0.5:
+                oracle.affine(a_s, b_s, lib=olib)
+                reps += 1
+            per_cfg["affine_small"]["cpu_baseline"] = {
+                "value": small_w.n * reps / (time.perf_counter() - t0), "unit": "elements/s",
+                "cores": 1, "kind": "oracle", "host_cores": host_cores(),
+                "sample": f"the full affine_small input x {reps} passes, sequential float64 "
+                          "loop, one thread"}
         # the same small scan replayed from a CUDA graph of 10 launches
         # (launch overhead amortised; inputs stay in L2 between launches)
         gs = torch.cuda.Stream(dev)
@@ -504,7 +575,7 @@ def run_ours(args, rank, world, local_rank):
         for name in ("s6_fp32", "s6_bf16", "s6_bidir", "s6_bf16_state", "s6_fp32_bwd",
                      "s6_bf16_bwd", "s6_bf16_layer"):
             per_cfg[name] = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream,
-                                     hbm_peak, sfu)
+                                     hbm_peak, sfu, cpu=not args.no_cpu)
         extras["per_config"] = per_cfg
 
     if rank != 0:
@@ -582,6 +653,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true",
+                    help="skip the oracle timings beside each S6 config")
     ap.add_argument("--affine-n", type=int, default=0,
                     help="with --workload affine_*: use this many elements (small ncu captures)")
     ap.add_argument("--workload", default=HEADLINE,

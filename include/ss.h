@@ -176,11 +176,22 @@ ss_status ss_affine_scan_host(const float *a, const float *b, float *h, int64_t 
  * make it before any stream capture on that device. Every call uses the same
  * array: calls that can run at the same time on the GPU (different streams,
  * or threads without ordering between them) race and must not be made.
- * Each call clears the array's error word on `stream`; device-detected
- * errors are not reported for this entry point.
+ * Each call clears the array's error word on `stream` when it starts; read a
+ * call's device-detected errors with ss_affine_scan_noalloc_status().
  */
 ss_status ss_affine_scan_noalloc(const float *a, const float *b, float *h, int64_t n,
                                  void *stream);
+
+/*
+ * Device-detected error of the last ss_affine_scan_noalloc call on the
+ * current device (a look-back wait that exceeded the spin timeout:
+ * SS_ERR_TIMEOUT, whose output is then undefined), or SS_OK. Synchronises
+ * `stream` first (pass the stream of that call), then reads and clears the
+ * error word of the library's static array; allocates nothing. The pages
+ * describing the method have no counterpart to it. SS_ERR_CUDA if the
+ * synchronisation or the read fails.
+ */
+ss_status ss_affine_scan_noalloc_status(void *stream);
 
 /* ------------------------------------------------------------ S6 */
 

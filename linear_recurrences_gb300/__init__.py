@@ -27,7 +27,8 @@ __all__ = [
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_testing_s6_plan", "ss_testing_s6_describe_plan",
-    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "SS_AFFINE_NOALLOC_MAX_N",
+    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_affine_scan_noalloc_status",
+    "SS_AFFINE_NOALLOC_MAX_N",
     "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
     "ss_selective_scan_layer_fwd", "ss_selective_scan_layer_workspace_bytes",
     "ss_affine_scan_log_step", "ss_affine_scan_state", "ss_affine_scan_host",
@@ -43,7 +44,8 @@ EXPORTED_SYMBOLS = (
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_testing_s6_plan", "ss_testing_s6_describe_plan",
-    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_selective_scan_fwd_state",
+    "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_affine_scan_noalloc_status",
+    "ss_selective_scan_fwd_state",
     "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
     "ss_selective_scan_layer_workspace_bytes", "ss_selective_scan_layer_fwd",
     "ss_affine_scan_log_step", "ss_affine_scan_state", "ss_affine_scan_host_workspace_bytes",
@@ -113,6 +115,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_probe_mufu_ex2.restype = ci
     L.ss_affine_scan_noalloc.argtypes = [vp, vp, vp, i64, vp]
     L.ss_affine_scan_noalloc.restype = ci
+    L.ss_affine_scan_noalloc_status.argtypes = [vp]
+    L.ss_affine_scan_noalloc_status.restype = ci
     L.ss_selective_scan_fwd_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64,
                                               i64, ci, ci, vp, sz, vp]
     L.ss_selective_scan_fwd_state.restype = ci
@@ -360,11 +364,23 @@ def ss_affine_scan_noalloc(a, b, h=None, stream=None):
     if h is None:
         h = torch.empty_like(a)
     _check_cuda(h, "h", (torch.float32,))
-    st = lib().ss_affine_scan_noalloc(_ptr(a), _ptr(b), _ptr(h), a.numel(),
-                                      _stream_handle(stream, a.device))
+    with torch.cuda.device(a.device):
+        st = lib().ss_affine_scan_noalloc(_ptr(a), _ptr(b), _ptr(h), a.numel(),
+                                          _stream_handle(stream, a.device))
     if st != SS_OK:
         raise SSError(st, "ss_affine_scan_noalloc")
     return h
+
+
+def ss_affine_scan_noalloc_status(stream=None, device=None) -> int:
+    """Synchronises `stream`, then reads and clears the device-side error word
+    of the static scratch used by ss_affine_scan_noalloc on `device` (the
+    current CUDA device by default): SS_OK or SS_ERR_TIMEOUT."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    with torch.cuda.device(dev):
+        return lib().ss_affine_scan_noalloc_status(_stream_handle(stream, dev))
 
 
 def ss_selective_scan_workspace_bytes(B, L, D, N, io_dtype=SS_F32, bidir=False) -> int:

@@ -42,6 +42,7 @@
 // always some CTA's current tile and every tile below it is finished, so its
 // look-back completes.
 #include <algorithm>
+#include <mutex>
 
 #include "ss_common.cuh"
 #include "ss_internal.h"
@@ -616,23 +617,46 @@ size_t affine_workspace_bytes(int64_t n) {
 
 namespace {
 
+// Per device: CTAs of each kernel variant that fit on one SM, and the SM
+// count. Filled on a device's first launch (which also raises the kernel's
+// dynamic shared-memory limit, a per-device attribute), under a lock.
+constexpr int kMaxDevices = 64;
+struct DeviceLaunch {
+    int sms = 0;
+    int per_sm[2] = {0, 0};  // [HS]
+};
+std::mutex g_launch_mutex;
+DeviceLaunch g_launch[kMaxDevices];
+
 template <bool HS>
 ss_status launch_variant(const AffineParams &prm, int64_t tiles, cudaStream_t stream) {
     // persistent grid: as many CTAs as fit at once, capped by the tile count
-    static int ctas_per_sm = -1, sms = 0;
-    if (ctas_per_sm < 0) {
-        int dev = 0, per_sm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaFuncSetAttribute(affine_scan_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kDynSmem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, affine_scan_kernel<HS>,
-                                                          kCtaThreads, kDynSmem) != cudaSuccess ||
-            per_sm < 1)
-            return SS_ERR_CUDA;
-        ctas_per_sm = per_sm;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SS_ERR_UNSUPPORTED;
+    int per_sm = 0, sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_launch_mutex);
+        DeviceLaunch &d = g_launch[dev];
+        if (d.per_sm[HS] <= 0) {
+            int n_sms = 0, n = 0;
+            if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaFuncSetAttribute(affine_scan_kernel<HS>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kDynSmem) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, affine_scan_kernel<HS>,
+                                                              kCtaThreads, kDynSmem) != cudaSuccess ||
+                n < 1 || n_sms < 1) {
+                cudaGetLastError();
+                return SS_ERR_CUDA;
+            }
+            d.sms = n_sms;
+            d.per_sm[HS] = n;
+        }
+        per_sm = d.per_sm[HS];
+        sms = d.sms;
     }
-    const long long grid = std::min<long long>(tiles, (long long)sms * ctas_per_sm);
+    const long long grid = std::min<long long>(tiles, (long long)sms * per_sm);
     affine_scan_kernel<HS><<<(unsigned)grid, kCtaThreads, kDynSmem, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }

@@ -12,9 +12,11 @@
 //
 // The array is shared by every call: it keeps the last call's descriptors,
 // whose launch tags make them harmless to the next call. Only the error word
-// must start each call at zero, so each call clears it on its stream. Two
-// calls that can overlap on the GPU (different streams, or different host
-// threads without ordering) race on the array and must not be issued.
+// must start each call at zero (a set word makes the look-back waits give
+// up), so each call clears it on its stream; ss_affine_scan_noalloc_status()
+// reads the last call's device-detected error from it. Two calls that
+// can overlap on the GPU (different streams, or different host threads
+// without ordering) race on the array and must not be issued.
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -28,7 +30,9 @@
 namespace {
 
 // Header plus one 32-byte descriptor per 4096-element tile, for up to
-// SS_AFFINE_NOALLOC_MAX_N elements (zero-filled at module load).
+// SS_AFFINE_NOALLOC_MAX_N elements (zero-filled at module load). Every call
+// also checks the scan's own workspace size against it, so a change of the
+// tile or descriptor size cannot make a call write past the array.
 constexpr size_t kScratchBytes = ss::kWsHeaderBytes + (size_t)(SS_AFFINE_NOALLOC_MAX_N / 4096) * 32;
 static __device__ __align__(256) unsigned char g_affine_scratch[kScratchBytes];
 
@@ -61,7 +65,8 @@ extern "C" ss_status ss_affine_scan_noalloc(const float *a, const float *b, floa
                                             void *stream) {
     if (n < 0) return SS_ERR_INVALID;
     if (n == 0) return SS_OK;
-    if (n > SS_AFFINE_NOALLOC_MAX_N) return SS_ERR_UNSUPPORTED;
+    if (n > SS_AFFINE_NOALLOC_MAX_N || ss::affine_workspace_bytes(n) > kScratchBytes)
+        return SS_ERR_UNSUPPORTED;
     if (!a || !b || !h) return SS_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) |
          reinterpret_cast<uintptr_t>(h)) & 3u)
@@ -73,5 +78,12 @@ extern "C" ss_status ss_affine_scan_noalloc(const float *a, const float *b, floa
     // a previous call's error word must not make this call's waits give up
     if (cudaMemsetAsync(&static_cast<ss::WsHeader *>(ws)->error, 0, sizeof(unsigned), s) != cudaSuccess)
         return SS_ERR_CUDA;
-    return ss::affine_launch(a, b, h, n, ws, s, ss::spin_timeout_ns(), -1);
+    return ss::affine_launch(a, b, h, n, ws, s, ss::spin_timeout_ns(), ss::take_skip_unit());
+}
+
+extern "C" ss_status ss_affine_scan_noalloc_status(void *stream) {
+    void *ws = nullptr;
+    const ss_status st = scratch_for_current_device(&ws);
+    if (st != SS_OK) return st;
+    return ss_get_device_status(ws, stream);
 }

@@ -12,8 +12,7 @@ namespace {
 std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
 std::atomic<long long> g_skip_unit{-1};
 
-// Consumes a pending ss_testing_skip_publish_once request (-1 if none).
-long long take_skip_unit() { return g_skip_unit.exchange(-1); }
+using ss::take_skip_unit;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -73,6 +72,7 @@ ss_status affine_entry(const float *a, const float *b, float *h, int64_t n, void
 
 namespace ss {
 unsigned long long spin_timeout_ns() { return g_timeout_ns.load(); }
+long long take_skip_unit() { return g_skip_unit.exchange(-1); }
 }  // namespace ss
 
 extern "C" {

@@ -72,6 +72,8 @@ struct S6Args {
 
 // Current bound on device-side waits (ss_set_spin_timeout_ns).
 unsigned long long spin_timeout_ns();
+// Consumes a pending ss_testing_skip_publish_once request (-1 if none).
+long long take_skip_unit();
 
 size_t s6_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int bidir);
 // Test hooks behind ss_testing_s6_plan / ss_testing_s6_describe_plan.

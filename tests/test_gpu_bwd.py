@@ -6,14 +6,18 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import require_gpu, to_dev, to_host_f64
+from gpu_util import rel_err, require_gpu, to_dev, to_host_f64
 
 pytestmark = pytest.mark.gpu
 THREADS = os.cpu_count() or 1
 NAMES = ("dx", "ddelta", "dA", "dBt", "dCt", "dDskip", "dh0")
-# max |g - ref| over a tensor, relative to max(1, max |ref|) of that tensor;
-# dx and ddelta are stored in the storage type, the rest in fp32
-TOL = {"f32": {k: 1e-4 for k in NAMES},
+# element-wise: max_i |g_i - ref_i| / max(1, |ref_i|) over each tensor;
+# dx and ddelta are stored in the storage type, the rest in fp32. ddelta and
+# dA are cancelling sums (ddelta over the 2N terms dh.(A a h) < 0 and
+# dh.(B x) of either sign, dA over all B*L steps), so their fp32 rounding error
+# scales with the sum of the terms' magnitudes, a few times |result|: each
+# gets 5x the fp32 bound of the others.
+TOL = {"f32": {**{k: 1e-4 for k in NAMES}, "ddelta": 5e-4, "dA": 5e-4},
        "bf16": {**{k: 1e-3 for k in NAMES}, "dx": 2e-2, "ddelta": 2e-2}}
 
 
@@ -28,8 +32,6 @@ def ss():
     return m
 
 
-def tensor_err(g, ref):
-    return float(np.max(np.abs(g - ref)) / max(1.0, float(np.max(np.abs(ref))))) if ref.size else 0.0
 
 
 def case(B, L, D, N, io="f32", softplus=False, state=True, seed=0):
@@ -67,7 +69,8 @@ def check(got, ref, io, skip_dh0=False):
     for k in NAMES:
         if skip_dh0 and k == "dh0":
             continue
-        err = tensor_err(got[k], ref[k])
+        assert got[k].shape == ref[k].shape, k
+        err = rel_err(got[k], ref[k])
         assert err <= TOL[io][k], f"{k}: {err:.3g} > {TOL[io][k]}"
 
 

@@ -157,20 +157,15 @@ def _sample_channels(B, D, count, seed):
 
 @pytest.mark.parametrize("name", ["s6_fp32", "s6_bf16", "s6_bidir"])
 def test_workload(torch, ss, name):
-    """Each S6 workload at full size, in the benchmark's launch configuration;
-    s6_fp32 is compared in full, the larger two on sampled channels."""
+    """Each S6 workload at full size, in the benchmark's launch configuration
+    (the library's own plan choice): every output element of every channel
+    against the oracle."""
     w = workloads.S6[name]
     inp = workloads.s6_workload_inputs(w)
     y = gpu_run(ss, torch, inp, w.softplus, w.bidir)
-    if name == "s6_fp32":
-        ref = oracle_run(inp, w.softplus, w.bidir)
-        assert rel_err(y, ref) <= TOL[w.io]
-        return
-    chans = _sample_channels(w.B, w.D, 160, seed=1)
-    ref = oracle.s6_channels(inp.x_f32, inp.delta_f32, inp.Bt_f32, inp.Ct_f32, inp.A, inp.Dskip,
-                             chans, softplus=w.softplus, bidir=w.bidir, threads=THREADS)
-    got = np.stack([y[c // w.D, :, c % w.D] for c in chans])
-    assert rel_err(got, ref) <= TOL[w.io]
+    ref = oracle_run(inp, w.softplus, w.bidir)
+    assert y.shape == ref.shape
+    assert rel_err(y, ref) <= TOL[w.io]
 
 
 @pytest.mark.parametrize("name", ["s6_fp32", "s6_bf16", "s6_bidir"])

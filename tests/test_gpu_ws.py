@@ -102,8 +102,11 @@ def test_variant_parity(torch, ss, ws_plan, shape, variant, io, softplus):
 def test_workload_every_element(torch, ss, ws_plan, name):
     """The fp32 and bf16 forward workloads at full size through the wavefront
     pass: every output element against the oracle."""
-    ws_plan(9, 8)
+    ws_plan(11, 4)
     w = workloads.S6[name]
+    io = ss.SS_BF16 if w.io == "bf16" else ss.SS_F32
+    kind, prm = ss.ss_testing_s6_describe_plan(w.B, w.L, w.D, w.N, io)
+    assert kind == 2 and prm[:2] == (11, 4)
     inp = workloads.s6_workload_inputs(w)
     dev = torch.device("cuda:0")
     t = lambda v: to_dev(v, dev, inp.io)
@@ -117,14 +120,14 @@ def test_workload_every_element(torch, ss, ws_plan, name):
 def test_unaligned_rows_fall_back(torch, ss, ws_plan):
     """D = 37 fp32 rows are not 16-byte multiples: the call takes the chunked
     kernel and stays correct."""
-    ws_plan(9, 8)
+    ws_plan(11, 4)
     inp = inputs(2, 300, 37, 16, "f32", False, seed=5)
     check(ss, torch, inp, False, with_h0=True, seed=5)
 
 
 def test_determinism_small(torch, ss, ws_plan):
     """Repeated calls are bitwise identical."""
-    ws_plan(9, 8)
+    ws_plan(11, 4)
     inp = inputs(2, 1500, 64, 16, "f32", True, seed=3)
     a, _ = run(ss, torch, inp, True)
     for _ in range(20):
