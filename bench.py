@@ -388,6 +388,37 @@ def s6_oracle_baseline(w, variant, inp, layer=None, elems_target=3_000_000):
                       f"once on {cores} threads (channels split across threads)"}
 
 
+def bench_proj_gemm(torch, ss, dev, steps, warmup, stream):
+    """The bf16 layer's projection GEMM alone (tcgen05 kernel, bias in the
+    epilogue) at the bf16 workload's layer shape: M = B*L = 32768, K = D =
+    1536, Nout = D + 2N = 1568; 2 M K Nout flops per call."""
+    import numpy as np
+    import workloads
+    w = workloads.S6["s6_bf16"]
+    M, K, Nout = w.B * w.L, w.D, w.D + 2 * w.N
+    g = np.random.Generator(np.random.PCG64(29))
+    x = torch.from_numpy(g.standard_normal((M, K)).astype(np.float32)).to(dev).to(torch.bfloat16)
+    W = torch.from_numpy((g.standard_normal((Nout, K)) / np.sqrt(K)).astype(np.float32)).to(
+        dev).to(torch.bfloat16)
+    bias = torch.from_numpy(g.normal(-4.0, 1.0, K).astype(np.float32)).to(dev)
+    out = torch.empty((M, Nout), dtype=torch.bfloat16, device=dev)
+    ws = ss.new_workspace(256, dev)
+    per, _ = time_launches(torch, lambda: ss.ss_testing_proj_gemm(x, W, bias=bias, out=out,
+                                                                  workspace=ws, stream=stream),
+                           steps, warmup, stream)
+    if ss.ss_get_device_status(ws) != ss.SS_OK:
+        raise RuntimeError("device reported an error in the projection GEMM")
+    ms = statistics.mean(per)
+    flops = 2.0 * M * K * Nout
+    peaks, kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"shape": [M, K, Nout], "ms": ms, "ms_min": min(per), "tflops": tf,
+            "bound": "tensor", "peak_tflops": peak, "peak_source": f"{kind} bf16_tflops",
+            "roofline_frac": tf / peak, "kernel": "proj_gemm_kernel (tcgen05, TMA, bias epilogue)",
+            "l2": "inputs (100 MB x + 4.8 MB W) near L2 size, no flush"}
+
+
 # ---------------------------------------------------------------- arms
 def run_reference(args, rank):
     if rank != 0:
@@ -572,6 +603,8 @@ def run_ours(args, rank, world, local_rank):
             "gbs": 12 * w.n / (lms * 1e-3) / 1e9, "roofline_frac": 12 * w.n / (lms * 1e-3) / 1e9 / hbm_peak,
             "kernel": "comparison: log-step (Hillis-Steele) tile scan, same look-back"}
         del lws
+        per_cfg["proj_gemm_bf16"] = bench_proj_gemm(torch, ss, dev, args.steps, args.warmup,
+                                                    stream)
         for name in ("s6_fp32", "s6_bf16", "s6_bidir", "s6_bf16_state", "s6_fp32_bwd",
                      "s6_bf16_bwd", "s6_bf16_layer"):
             per_cfg[name] = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream,
@@ -625,6 +658,8 @@ def run_single(args):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         sfu = mufu_probe(torch, ss, dev, sms) if not args.no_extras else 9.86e12
         r = bench_s6(torch, ss, dev, name, args.steps, args.warmup, stream, hbm_peak, sfu)
+    elif name == "proj_gemm_bf16":
+        r = bench_proj_gemm(torch, ss, dev, args.steps, args.warmup, stream)
     elif name in workloads.AFFINE or (name.endswith("_log_step") and name[:-9] in workloads.AFFINE):
         log_step = name.endswith("_log_step")
         name = name[:-9] if log_step else name
@@ -660,7 +695,7 @@ def main():
     ap.add_argument("--workload", default=HEADLINE,
                     help="time one workload only (affine_small, affine_large, s6_fp32, "
                          "affine_large_log_step, s6_bf16, s6_bidir, s6_bf16_state, s6_fp32_bwd, s6_bf16_bwd, "
-                         "s6_bf16_layer); "
+                         "s6_bf16_layer, proj_gemm_bf16); "
                          "the default "
                          "is the full benchmark")
     args = ap.parse_args()

@@ -54,6 +54,21 @@ void ss_testing_s6_plan(int kind, int a, int b, int c);
 int ss_testing_s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,
                                 int bidir, int64_t *out);
 
+/*
+ * Runs the layer's projection GEMM alone, so tests can compare it with the
+ * oracle's projections directly: out (M x Nout bf16, row stride ld_out
+ * elements) = x (M x K bf16, row-major) times W (Nout x K bf16, row-major)
+ * transposed, fp32 accumulation, bias[j] (fp32, device) added to columns
+ * j < n_bias (bias may be null) before the one rounding to bf16.
+ * workspace: a zero-filled device block of at least 256 bytes (its header
+ * takes device errors, read with ss_get_device_status). Returns
+ * SS_ERR_UNSUPPORTED unless K and ld_out are multiples of 8, ld_out >= Nout
+ * and x, W, out are 16-byte aligned. Asynchronous on `stream`.
+ */
+int ss_testing_proj_gemm(const void *x, const void *W, void *out, const float *bias,
+                         int64_t n_bias, int64_t M, int64_t K, int64_t Nout, int64_t ld_out,
+                         void *workspace, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

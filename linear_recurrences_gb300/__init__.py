@@ -26,7 +26,7 @@ __all__ = [
     "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
-    "ss_testing_s6_plan", "ss_testing_s6_describe_plan",
+    "ss_testing_s6_plan", "ss_testing_s6_describe_plan", "ss_testing_proj_gemm",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_affine_scan_noalloc_status",
     "SS_AFFINE_NOALLOC_MAX_N",
     "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
@@ -43,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "ss_status_string", "ss_abi_version", "ss_affine_scan_workspace_bytes", "ss_affine_scan",
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
-    "ss_testing_s6_plan", "ss_testing_s6_describe_plan",
+    "ss_testing_s6_plan", "ss_testing_s6_describe_plan", "ss_testing_proj_gemm",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_affine_scan_noalloc_status",
     "ss_selective_scan_fwd_state",
     "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
@@ -111,6 +111,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_testing_s6_describe_plan.argtypes = [i64, i64, i64, i64, ci, ci,
                                               ctypes.POINTER(ctypes.c_int64)]
     L.ss_testing_s6_describe_plan.restype = ci
+    L.ss_testing_proj_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp]
+    L.ss_testing_proj_gemm.restype = ci
     L.ss_probe_mufu_ex2.argtypes = [vp, ci, ci, vp]
     L.ss_probe_mufu_ex2.restype = ci
     L.ss_affine_scan_noalloc.argtypes = [vp, vp, vp, i64, vp]
@@ -184,6 +186,35 @@ def ss_testing_s6_describe_plan(B, L, D, N, io_dtype=SS_F32, bidir=False):
     k = lib().ss_testing_s6_describe_plan(int(B), int(L), int(D), int(N), int(io_dtype),
                                           int(bool(bidir)), out)
     return k, tuple(out)
+
+
+def ss_testing_proj_gemm(x, W, bias=None, out=None, ld_out=None, workspace=None, stream=None):
+    """Test hook (include/ss_testing.h): the layer's projection GEMM alone.
+    x (M, K) and W (Nout, K) bf16 CUDA tensors; bias fp32 (n_bias,) added to
+    the first n_bias columns; returns out (M, ld_out) bf16 (columns >= Nout
+    untouched)."""
+    torch = _torch()
+    _check_cuda(x, "x", (torch.bfloat16,))
+    _check_cuda(W, "W", (torch.bfloat16,))
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1] or x.device != W.device:
+        raise ValueError("x must be (M, K) and W (Nout, K) on one device")
+    M, K = x.shape
+    Nout = W.shape[0]
+    ld = int(ld_out) if ld_out is not None else Nout
+    if out is None:
+        out = torch.zeros((M, ld), dtype=torch.bfloat16, device=x.device)
+    _check_cuda(out, "out", (torch.bfloat16,))
+    if bias is not None:
+        _check_cuda(bias, "bias", (torch.float32,))
+    if workspace is None:
+        workspace = new_workspace(256, x.device)
+    with torch.cuda.device(x.device):
+        st = lib().ss_testing_proj_gemm(_ptr(x), _ptr(W), _ptr(out), _ptr(bias),
+                                        0 if bias is None else bias.numel(), M, K, Nout, ld,
+                                        _ptr(workspace), _stream_handle(stream, x.device))
+    if st != SS_OK:
+        raise SSError(st, "ss_testing_proj_gemm")
+    return out
 
 
 def ss_probe_mufu_ex2(out, blocks: int, iters: int, stream=None) -> None:

@@ -4,11 +4,14 @@
 // delta = softplus(proj_delta(x)) with a bias, B_t = proj_B(x), C_t =
 // proj_C(x), then the S6 recurrence. The three projections are one dense
 // GEMM: x ((B*L) x D) times the stacked weights W_proj ((D + 2N) x D)
-// transposed, a single cuBLASLt matmul (bf16 or fp32 inputs, fp32
-// accumulation) into one (B*L) x (D + 2N) workspace buffer whose row holds
-// the pre-activation, B_t and C_t of one step; the scan reads the three
-// column blocks in place at that row stride, with the delta bias and
-// softplus fused in.
+// transposed, into one (B*L) x ld workspace buffer whose row holds the
+// pre-activation, B_t and C_t of one step; the scan reads the three column
+// blocks in place at that row stride, with softplus fused in.
+//  * bf16: the hand-written tensor-core GEMM (proj_gemm.cu) adds the delta
+//    bias to the fp32 accumulator and rounds once to bf16, as a bf16 Linear
+//    layer does; rows are padded to a multiple of 8 elements (16 bytes).
+//  * fp32: a cuBLASLt fp32 GEMM (full fp32 products and sums; the tensor
+//    cores have no fp32-exact mode) and the scan adds the bias in fp32.
 #include <cublasLt.h>
 
 #include <algorithm>
@@ -81,18 +84,20 @@ ss_status gemm_xwT(const void *x, const void *W, void *out, int64_t M, int64_t K
 
 struct LayerPlan {
     size_t proj, lt, scan, total;  // section offsets, then total bytes
+    int64_t ld;                    // row stride (elements) of the projections
 };
 
 LayerPlan layer_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16) {
     LayerPlan pl{};
     const size_t es = io_bf16 ? 2 : 4;
     const size_t M = (size_t)(B * L);
+    pl.ld = io_bf16 ? (D + 2 * N + 7) / 8 * 8 : D + 2 * N;
     // the scan's section comes first, so the workspace starts with its
     // header (error word) even when the scan needs no further workspace
     pl.scan = 0;
     pl.proj = std::max<size_t>(kWsHeaderBytes, align256(s6_workspace_bytes(B, L, D, N, io_bf16, 0)));
-    pl.lt = pl.proj + align256(M * (size_t)(D + 2 * N) * es);
-    pl.total = pl.lt + kLtWorkspace;
+    pl.lt = pl.proj + align256(M * (size_t)pl.ld * es);
+    pl.total = pl.lt + (io_bf16 ? 0 : kLtWorkspace);
     return pl;
 }
 
@@ -116,20 +121,27 @@ ss_status layer_fwd_launch(const void *x, const void *W_proj, const float *b_del
     const int64_t M = B * L;
     // rows [0, D) of W_proj: proj_delta; [D, D + N): proj_B; [D + N, D + 2N):
     // proj_C, so output row m is (pre-activation, B_t, C_t) of step m
-    const ss_status st =
-        gemm_xwT(x, W_proj, ws + pl.proj, M, D, D + 2 * N, io_bf16, ws + pl.lt, stream);
+    ss_status st;
+    if (io_bf16) {
+        if (!proj_gemm_supported(x, W_proj, ws + pl.proj, M, D, D + 2 * N, pl.ld))
+            return SS_ERR_UNSUPPORTED;
+        st = proj_gemm_launch(x, W_proj, ws + pl.proj, b_delta, D, M, D, D + 2 * N, pl.ld, ws,
+                              stream, timeout_ns);
+    } else {
+        st = gemm_xwT(x, W_proj, ws + pl.proj, M, D, D + 2 * N, false, ws + pl.lt, stream);
+    }
     if (st != SS_OK) return st;
     S6Args a;
     a.x = x;
     a.delta = ws + pl.proj;
     a.Bt = ws + pl.proj + (size_t)D * es;
     a.Ct = ws + pl.proj + (size_t)(D + N) * es;
-    a.ld_delta = D + 2 * N;
-    a.ld_bc = D + 2 * N;
+    a.ld_delta = pl.ld;
+    a.ld_bc = pl.ld;
     a.A = A;
     a.Dskip = Dskip;
     a.y = y;
-    a.delta_bias = b_delta;
+    a.delta_bias = io_bf16 ? nullptr : b_delta;  // bf16: added in the GEMM epilogue
     a.h0 = nullptr;
     a.h_last = nullptr;
     a.B = B;

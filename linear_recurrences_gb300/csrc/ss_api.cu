@@ -273,6 +273,16 @@ void ss_testing_skip_publish_once(int64_t unit) { g_skip_unit.store(unit < 0 ? -
 
 void ss_testing_s6_plan(int kind, int a, int b, int c) { ss::s6_set_plan_override(kind, a, b, c); }
 
+int ss_testing_proj_gemm(const void *x, const void *W, void *out, const float *bias,
+                         int64_t n_bias, int64_t M, int64_t K, int64_t Nout, int64_t ld_out,
+                         void *workspace, void *stream) {
+    if (M < 0 || K < 0 || Nout < 0 || n_bias < 0) return SS_ERR_INVALID;
+    if (M == 0 || Nout == 0) return SS_OK;
+    if (!x || !W || !out || !workspace || !aligned(workspace, 256)) return SS_ERR_INVALID;
+    return ss::proj_gemm_launch(x, W, out, bias, n_bias, M, K, Nout, ld_out, workspace,
+                                static_cast<cudaStream_t>(stream), g_timeout_ns.load());
+}
+
 int ss_testing_s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,
                                 int bidir, int64_t *out) {
     if (!out || (io_dtype != SS_F32 && io_dtype != SS_BF16)) return -1;

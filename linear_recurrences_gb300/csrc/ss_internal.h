@@ -35,10 +35,25 @@ inline int device_smem_per_sm() {
 // runtime's driver entry point) into `map` (a 128-byte CUtensorMap): `rank`
 // dimensions innermost first, dims[i] elements each, strides[i] bytes
 // between consecutive indices of dimension i + 1, box[i] elements per copy,
-// fp32 or bf16 elements, no swizzle, zero fill outside the extent. false if
-// the entry point is missing or the driver rejects the layout.
+// fp32 or bf16 elements, zero fill outside the extent; swizzle128: the
+// 128-byte shared-memory swizzle (the box's inner extent must be 128 bytes),
+// else none. false if the entry point is missing or the driver rejects the
+// layout.
 bool encode_tiled_map(void *map, const void *base, bool bf16, int rank, const uint64_t *dims,
-                      const uint64_t *strides, const uint32_t *box);
+                      const uint64_t *strides, const uint32_t *box, bool swizzle128 = false);
+
+// Projection GEMM on the tensor cores (tcgen05): out (M x Nout, row stride
+// ld_out, bf16) = x (M x K, bf16, row-major) times W (Nout x K, bf16,
+// row-major) transposed, fp32 accumulation, bias[j] (fp32) added to columns
+// j < n_bias before the single rounding to bf16 (bias may be null).
+// workspace: a 256-byte workspace header (device errors). Supported when
+// proj_gemm_supported() holds: K and ld_out multiples of 8 elements, the
+// three pointers 16-byte aligned.
+bool proj_gemm_supported(const void *x, const void *W, const void *out, int64_t M, int64_t K,
+                         int64_t Nout, int64_t ld_out);
+ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float *bias,
+                           int64_t n_bias, int64_t M, int64_t K, int64_t Nout, int64_t ld_out,
+                           void *workspace, cudaStream_t stream, unsigned long long timeout_ns);
 
 size_t affine_workspace_bytes(int64_t n);
 // log_step_tiles: scan each tile with the log-step (Hillis-Steele) algorithm

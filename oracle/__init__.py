@@ -233,6 +233,23 @@ def _round_bf16(v):
     return np.ldexp(np.round(m * 256.0) / 256.0, e)
 
 
+def projections(x2d, W_proj, bias, io="f32") -> np.ndarray:
+    """x2d (M, K) times W_proj (n_out, K) transposed, plus bias (n_bias <=
+    n_out values) on the first n_bias columns: a float64 product of the exact
+    input values, the bias added before the single rounding to the storage
+    type (float32, or bfloat16 with io == "bf16"), as a Linear layer with a
+    bias returns it. Returns (M, n_out) float64 holding the rounded values."""
+    x2d = np.ascontiguousarray(x2d, dtype=np.float32).astype(np.float64)
+    W = np.ascontiguousarray(W_proj, dtype=np.float32).astype(np.float64)
+    P = x2d @ W.T
+    if bias is not None:
+        b = np.ascontiguousarray(bias, dtype=np.float32).astype(np.float64)
+        P[:, :b.shape[0]] += b
+    if io == "bf16":
+        return _round_bf16(P)
+    return P.astype(np.float32).astype(np.float64)
+
+
 def layer_fwd(x, W_proj, b_delta, A, Dskip, io="f32", threads=1,
               lib: ctypes.CDLL | None = None):
     """The selective-scan layer's forward pass ("POPCORNBENCH FW-GLM-5-1
@@ -240,22 +257,22 @@ def layer_fwd(x, W_proj, b_delta, A, Dskip, io="f32", threads=1,
     projections, then the scan. W_proj is (D + 2N, D), PyTorch Linear layout:
     rows [0, D) proj_delta, [D, D + N) proj_B, [D + N, D + 2N) proj_C.
         delta = softplus(x W_delta^T + b_delta),  B_t = x W_B^T,  C_t = x W_C^T
-    The projections are float64 matrix products of the exact input values;
-    their results enter the float64 scan loop rounded once to float32 (the
-    loop's input type). With io == "bf16" the projections are first rounded
-    once to bfloat16, as a Linear layer in that storage type returns them;
-    the delta bias is added after that rounding. Returns y (B, L, D) float64."""
+    The projections are float64 matrix products of the exact input values,
+    the delta bias added to the pre-activation before any rounding (a Linear
+    layer adds its bias to the accumulated product); the results enter the
+    float64 scan loop rounded once to float32 (the loop's input type), or,
+    with io == "bf16", rounded once to bfloat16, as a Linear layer in that
+    storage type returns them. Returns y (B, L, D) float64."""
     x = _f32(x)
-    W = np.ascontiguousarray(W_proj, dtype=np.float32).astype(np.float64)
+    W = np.ascontiguousarray(W_proj, dtype=np.float32)
     B, L, D = x.shape
     N = (W.shape[0] - D) // 2
     if W.shape != (D + 2 * N, D) or N < 1:
         raise ValueError("W_proj must be (D + 2N, D)")
-    b = np.ascontiguousarray(b_delta, dtype=np.float32).astype(np.float64)
-    P = x.astype(np.float64).reshape(B * L, D) @ W.T                   # (B*L, D + 2N)
-    if io == "bf16":
-        P = _round_bf16(P)
-    pre = (P[:, :D] + b).reshape(B, L, D).astype(np.float32)
+    if np.shape(b_delta) != (D,):
+        raise ValueError("b_delta must be (D,)")
+    P = projections(x.reshape(B * L, D), W, b_delta, io)               # (B*L, D + 2N)
+    pre = P[:, :D].reshape(B, L, D).astype(np.float32)
     Bt = P[:, D:D + N].reshape(B, L, N).astype(np.float32)
     Ct = P[:, D + N:].reshape(B, L, N).astype(np.float32)
     return s6_fwd(x, pre, Bt, Ct, A, Dskip, softplus=True, threads=threads, lib=lib)

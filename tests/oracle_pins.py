@@ -556,8 +556,32 @@ def pin_bf16_rounding(lib):
     assert r(np.array([-(1.0 + 2.0 ** -8 + 2.0 ** -30)]))[0] == -(1.0 + 2.0 ** -7)
 
 
+def pin_layer_bf16_bias_before_rounding(lib):
+    """Hand-worked bf16 layer step where the place of the bias decides the
+    result. D = 2, N = 1, one step, x = (1, 1), W_delta row 0 = (1, 2^-8),
+    row 1 = 0, W_B = W_C = (1, 0), b_delta = (2^-8, 0), A = -1, D = 0:
+    proj_delta(x)_0 = 1 + 2^-8 and, with the bias, 1 + 2^-7, which bfloat16
+    holds exactly; B_t = C_t = 1. A Linear layer adds the bias before its one
+    rounding, so delta_0 = softplus(1 + 2^-7) and y_0 = delta_0 * B x_0 * C
+    = softplus(1 + 2^-7); rounding first would give bf16(1 + 2^-8) = 1 (a
+    tie, to even) and softplus(1 + 2^-8). Channel 1: y_1 = softplus(0) = ln 2.
+    In float32 the same weights give the unrounded value."""
+    x = np.array([[[1.0, 1.0]]], np.float32)
+    W = np.array([[1.0, 2.0 ** -8], [0.0, 0.0], [1.0, 0.0], [1.0, 0.0]], np.float32)
+    bd = np.array([2.0 ** -8, 0.0], np.float32)
+    A = np.array([[-1.0], [-1.0]], np.float32)
+    Ds = np.zeros(2, np.float32)
+    sp = lambda v: math.log1p(math.exp(v))
+    y = oracle.layer_fwd(x, W, bd, A, Ds, io="bf16", lib=lib)
+    assert abs(y[0, 0, 0] - sp(1.0 + 2.0 ** -7)) <= 1e-12, "bf16: bias before the rounding"
+    assert abs(y[0, 0, 1] - math.log(2.0)) <= 1e-12, "bf16: zero pre-activation"
+    y = oracle.layer_fwd(x, W, bd, A, Ds, io="f32", lib=lib)
+    assert abs(y[0, 0, 0] - sp(1.0 + 2.0 ** -7)) <= 1e-12, "f32: 1 + 2^-7 is exact too"
+
+
 BWD_PINS = [pin_bwd_finite_differences, pin_bwd_finite_differences_softplus,
-            pin_bwd_euler_and_skip, pin_layer_wiring, pin_bf16_rounding]
+            pin_bwd_euler_and_skip, pin_layer_wiring, pin_bf16_rounding,
+            pin_layer_bf16_bias_before_rounding]
 ALL_PINS = ALL_PINS + BWD_PINS
 
 

@@ -173,3 +173,33 @@ def s6_inputs(B: int, L: int, D: int, N: int, *, io: str = "f32",
 def s6_workload_inputs(w: S6Workload, seed: int = SEED) -> S6Inputs:
     return s6_inputs(w.B, w.L, w.D, w.N, io=w.io, delta=w.delta,
                      dskip=w.dskip, seed=seed)
+
+
+# ---------------------------------------------------------------- layer
+def layer_inputs(B: int, L: int, D: int, N: int, *, io: str = "f32", seed: int = SEED):
+    """Inputs of the selective-scan layer (projections, then the scan):
+    x (B, L, D), W_proj (D + 2N, D) in Linear layout (rows: proj_delta,
+    proj_B, proj_C), b_delta (D,), A (D, N), Dskip (D,), all float32 arrays
+    holding the values the kernels see. x ~ N(0, 1), W ~ N(0, 1/D) (unit-
+    variance projections), b_delta ~ N(-4, 1) (softplus gives small steps, as
+    in the bf16 workload), A ~ -U(0.1, 4), Dskip ~ N(0, 1).
+
+    io == "bf16" puts every value on a grid on which a projection sum is
+    exact in fp32 whatever the order of its terms: x on multiples of 2^-5
+    inside (-4, 4); W rounded to bf16 with magnitudes below 2^-8 set to 0 (so
+    every product is a multiple of 2^-20); b_delta on multiples of 2^-20. The
+    projections stay far below 16 in magnitude, so the fp32 sums are exact and
+    the one rounding to bf16 sees the same value on every side."""
+    g = generator(seed)
+    x = g.standard_normal((B, L, D))
+    W = g.standard_normal((D + 2 * N, D)) / np.sqrt(D)
+    b = g.normal(-4.0, 1.0, D)
+    A = -g.uniform(0.1, 4.0, (D, N))
+    Ds = g.standard_normal(D)
+    if io == "bf16":
+        x = np.clip(np.round(x * 32.0), -127, 127) / 32.0
+        W = bf16_bits_to_f32(f32_to_bf16_bits(W.astype(np.float32))).astype(np.float64)
+        W[np.abs(W) < 2.0 ** -8] = 0.0
+        b = np.round(b * 2.0 ** 20) / 2.0 ** 20
+    f = lambda v: np.ascontiguousarray(v, dtype=np.float32)
+    return f(x), f(W), f(b), f(A), f(Ds)
