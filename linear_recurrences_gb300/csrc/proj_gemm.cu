@@ -24,9 +24,14 @@
 //             (tile rows), 32 columns per tcgen05.ld, adds the bias, rounds
 //             to bf16 and stores 64 contiguous bytes of its row per chunk.
 // With two accumulators the epilogue of one tile runs under the main loop
-// of the next. Tiles go to CTAs round-robin in (M-block, N-block) order, so
-// the CTAs working at one time share their x tiles through L2; W stays in
-// L2 throughout.
+// of the next. CTAs run in clusters of two on neighbouring SMs: the pair
+// takes two M-blocks of the same N-block at a time, each CTA loads its own
+// x tile and half of the shared W tile, multicast into both CTAs' shared
+// memory, so each W byte leaves L2 once per pair (a stage is refilled only
+// after both CTAs' MMAs have read it: each MMA thread's commit arrives on
+// both CTAs' stage barriers). Pairs take (M-block pair, N-block) tiles
+// round-robin, so the pairs working at one time share their x tiles through
+// L2; W stays in L2 throughout.
 //
 // Every wait is bounded: on timeout the CTA records SS_ERR_TIMEOUT in the
 // workspace header, every role leaves its loop, the producer waits (bounded)
@@ -110,6 +115,36 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
                  ::"r"(smem_addr(bar)) : "memory");
 }
 
+// As umma_commit, arriving on `bar` at the same offset in every CTA of the
+// cluster named in `mask`.
+__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)), "h"(mask) : "memory");
+}
+
+// 2D tile copy into `dst` (and the same offset) of every CTA of the cluster in
+// `mask`, completing on `bar` at the same offset in each.
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const void *tmap, int x, int y,
+                                               uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y),
+          "r"(smem_addr(bar)), "h"(mask) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -153,6 +188,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, unsigned parity, co
 }
 
 // ---------------------------------------------------------------- kernel
+// PAIR: clusters of two CTAs sharing the W tile (see the top of the file);
+// otherwise every CTA loads its own tiles.
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ GemmShared sh;
@@ -161,11 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const size_t stage_bytes = kATileBytes + (size_t)p.BN * kBK * 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // work units: (M-block, N-block) tiles, or (M-block pair, N-block) per cluster
+    const unsigned rank = PAIR ? cluster_rank() : 0u;
+    const long long unit0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
+    const long long unit_step = PAIR ? gridDim.x / 2 : gridDim.x;
+    auto m_block = [&](long long u) { return PAIR ? 2 * (u / p.n_tiles_n) + rank : u / p.n_tiles_n; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.empty[s], PAIR ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sh.acc_full[a], 1);
@@ -181,7 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         tc_fence_before();
     }
-    __syncthreads();
+    if (PAIR)
+        cluster_sync();  // the peer's barriers are initialised before any multicast
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
@@ -192,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
             unsigned phase = 0;
             long long issued = 0;
             bool ok = true;
-            for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-                const int m0 = (int)(t / p.n_tiles_n) * kBM;
-                const int n0 = (int)(t % p.n_tiles_n) * p.BN;
+            for (long long u = unit0; ok && u < p.num_tiles; u += unit_step) {
+                const int m0 = (int)m_block(u) * kBM;
+                const int n0 = (int)(u % p.n_tiles_n) * p.BN;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!wait_or_abort(&sh.empty[stage], phase ^ 1u, p, sh, 1u)) {
                         ok = false;
@@ -203,7 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                     uint8_t *sa = smem + stage * stage_bytes;
                     mbar_arrive_expect_tx(&sh.full[stage], (unsigned)stage_bytes);
                     tma_load_2d(sa, &p.tm_a, kb * kBK, m0, &sh.full[stage]);
-                    tma_load_2d(sa + kATileBytes, &p.tm_b, kb * kBK, n0, &sh.full[stage]);
+                    if (PAIR) {  // this CTA's half of the W tile, into both CTAs
+                        const int half = p.BN / 2;
+                        tma_load_2d_mc(sa + kATileBytes + (size_t)rank * half * kBK * 2, &p.tm_b,
+                                       kb * kBK, n0 + (int)rank * half, &sh.full[stage], 0x3);
+                    } else {
+                        tma_load_2d(sa + kATileBytes, &p.tm_b, kb * kBK, n0, &sh.full[stage]);
+                    }
                     ++issued;
                     if (++stage == p.stages) {
                         stage = 0;
@@ -226,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
             unsigned acc_phase = 0;
             bool ok = true;
             const uint32_t smem0 = smem_addr(smem);
-            for (long long t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (long long u = unit0; ok && u < p.num_tiles; u += unit_step) {
                 if (!wait_or_abort(&sh.acc_empty[acc], acc_phase ^ 1u, p, sh, 2u)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
@@ -242,7 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                     for (int k = 0; k < kBK / kUmmaK; ++k)
                         umma_bf16(d_tmem, sw128_desc(sa + k * kUmmaK * 2),
                                   sw128_desc(sb + k * kUmmaK * 2), p.idesc, (kb | k) != 0);
-                    umma_commit(&sh.empty[stage]);  // stage free once these MMAs read it
+                    // stage free once these MMAs read it (in both CTAs of a pair)
+                    if (PAIR)
+                        umma_commit_mc(&sh.empty[stage], 0x3);
+                    else
+                        umma_commit(&sh.empty[stage]);
                     if (++stage == p.stages) {
                         stage = 0;
                         phase ^= 1u;
@@ -263,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         const int quarter = warp & 3;  // tensor-memory lanes 32 quarter .. + 31
         int acc = 0;
         unsigned acc_phase = 0;
-        for (long long t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        for (long long u = unit0; u < p.num_tiles; u += unit_step) {
             // warp-uniform outcome: tcgen05.ld below is warp-collective
             if (!__all_sync(0xffffffffu, wait_or_abort(&sh.acc_full[acc], acc_phase, p, sh, 4u)))
                 break;
             tc_fence_after();
-            const long long row = (t / p.n_tiles_n) * kBM + quarter * 32 + lane;
-            const int n0 = (int)(t % p.n_tiles_n) * p.BN;
+            const long long row = m_block(u) * kBM + quarter * 32 + lane;
+            const int n0 = (int)(u % p.n_tiles_n) * p.BN;
             __nv_bfloat16 *orow = p.out + row * p.ld_out;
             for (int c = 0; c < p.BN; c += 32) {
                 uint32_t r[32];
@@ -319,12 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                      ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
+    // neither CTA of a pair leaves while the other may still multicast into
+    // its shared memory or arrive on its barriers
+    if (PAIR) cluster_sync();
 }
 
 // ---------------------------------------------------------------- planning
 struct GemmPlan {
     int BN, n_tiles_n, stages, k_blocks;
-    long long num_tiles;
+    long long num_tiles;  // work units: tiles, or tile pairs when pair
+    bool pair;
     size_t smem;
 };
 
@@ -334,7 +394,10 @@ GemmPlan plan_gemm(int64_t M, int64_t K, int64_t Nout) {
     const int64_t per = (Nout + g.n_tiles_n - 1) / g.n_tiles_n;
     g.BN = (int)((per + 31) / 32 * 32);
     g.k_blocks = (int)((K + kBK - 1) / kBK);
-    g.num_tiles = ((M + kBM - 1) / kBM) * g.n_tiles_n;
+    const int64_t m_tiles = (M + kBM - 1) / kBM;
+    // pairs need two M-blocks and W half-tiles of whole 8-row swizzle atoms
+    g.pair = m_tiles >= 2 && (g.BN / 2) % 8 == 0;
+    g.num_tiles = (g.pair ? (m_tiles + 1) / 2 : m_tiles) * g.n_tiles_n;
     const size_t stage_bytes = kATileBytes + (size_t)g.BN * kBK * 2;
     g.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - 1024) / stage_bytes);
     g.smem = 1024 + (size_t)g.stages * stage_bytes;
@@ -368,7 +431,7 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
     {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)Nout};
         const uint64_t strides[1] = {(uint64_t)K * 2};
-        const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)g.BN};
+        const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)(g.pair ? g.BN / 2 : g.BN)};
         if (!encode_tiled_map(&prm.tm_b, W, true, 2, dims, strides, box, true))
             return SS_ERR_UNSUPPORTED;
     }
@@ -391,11 +454,40 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
     // 17-22, M >> 4 in bits 24-28
     prm.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((unsigned)(g.BN >> 3) << 17) |
                 ((unsigned)(kBM >> 4) << 24);
-    if (cudaFuncSetAttribute(proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!g.pair) {
+        if (cudaFuncSetAttribute(proj_gemm_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)g.smem) != cudaSuccess)
+            return SS_ERR_CUDA;
+        const long long grid = std::min<long long>(g.num_tiles, device_sm_count());
+        proj_gemm_kernel<false><<<(unsigned)grid, kThreads, g.smem, stream>>>(prm);
+        return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+    }
+    if (cudaFuncSetAttribute(proj_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)g.smem) != cudaSuccess)
         return SS_ERR_CUDA;
-    const long long grid = std::min<long long>(g.num_tiles, device_sm_count());
-    proj_gemm_kernel<<<(unsigned)grid, kThreads, g.smem, stream>>>(prm);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = g.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many pairs as can be resident at once (all CTAs of a persistent
+    // grid run together), capped by the work
+    int clusters = 0;
+    cfg.gridDim = dim3(2 * (unsigned)std::max(1, device_sm_count() / 2), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&clusters, proj_gemm_kernel<true>, &cfg) != cudaSuccess ||
+        clusters < 1) {
+        cudaGetLastError();
+        return SS_ERR_CUDA;
+    }
+    cfg.gridDim = dim3(2 * (unsigned)std::min<long long>(g.num_tiles, clusters), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, proj_gemm_kernel<true>, prm) != cudaSuccess) return SS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
