@@ -168,6 +168,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Eight bf16 values to dst (16-byte aligned); only the first `valid` when
+// fewer than eight columns remain in the row (padding columns stay untouched).
+__device__ __forceinline__ void store_chunk(__nv_bfloat16 *dst, uint4 w, int valid) {
+    if (valid >= 8) {
+        *reinterpret_cast<uint4 *>(dst) = w;
+        return;
+    }
+    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j < valid)
+            reinterpret_cast<unsigned short *>(dst)[j] = (unsigned short)(wd[j >> 1] >> (16 * (j & 1)));
+}
+
 // Waits for phase `parity` of `bar`; false once the CTA is aborting or the
 // wait outlived the launch's timeout (which starts the abort).
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, unsigned parity, const GemmParams &p,
@@ -316,6 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         }
     } else {
         // ------------------------------------------------ epilogue
+        // Lane = tile row: each 32-column chunk leaves as four 16-byte stores
+        // per lane (64 contiguous bytes of its row). Staging the rows through
+        // shared memory to store whole row segments per instruction measured
+        // slower (it takes a pipeline stage's worth of shared memory).
         const int quarter = warp & 3;  // tensor-memory lanes 32 quarter .. + 31
         int acc = 0;
         unsigned acc_phase = 0;
@@ -324,9 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
             if (!__all_sync(0xffffffffu, wait_or_abort(&sh.acc_full[acc], acc_phase, p, sh, 4u)))
                 break;
             tc_fence_after();
-            const long long row = m_block(u) * kBM + quarter * 32 + lane;
+            const long long row0 = m_block(u) * kBM + quarter * 32;
             const int n0 = (int)(u % p.n_tiles_n) * p.BN;
-            __nv_bfloat16 *orow = p.out + row * p.ld_out;
             for (int c = 0; c < p.BN; c += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kAccCols + c), r);
@@ -335,31 +352,30 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 if (p.bias && col0 < p.n_bias) {
+                    // lane j fetches the bias of column col0 + j (one coalesced
+                    // load), every lane takes the 32 values by shuffle
+                    const float bj = col0 + lane < p.n_bias ? __ldg(p.bias + col0 + lane) : 0.0f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (col0 + j < p.n_bias) v[j] += __ldg(p.bias + col0 + j);
+                    for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, bj, j);
                 }
-                if (row < p.M) {
-                    if (col0 + 32 <= p.Nout) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 w;
-                            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
-                            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-                            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-                            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-                            w.x = *reinterpret_cast<uint32_t *>(&h0);
-                            w.y = *reinterpret_cast<uint32_t *>(&h1);
-                            w.z = *reinterpret_cast<uint32_t *>(&h2);
-                            w.w = *reinterpret_cast<uint32_t *>(&h3);
-                            *reinterpret_cast<uint4 *>(orow + col0 + 8 * q) = w;
-                        }
-                    } else {
-                        for (int j = 0; j < 32; ++j)
-                            if (col0 + j < p.Nout) orow[col0 + j] = __float2bfloat16_rn(v[j]);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w;
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
+                    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+                    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+                    w.x = *reinterpret_cast<uint32_t *>(&h0);
+                    w.y = *reinterpret_cast<uint32_t *>(&h1);
+                    w.z = *reinterpret_cast<uint32_t *>(&h2);
+                    w.w = *reinterpret_cast<uint32_t *>(&h3);
+                    const long long row = row0 + lane;
+                    const int col = col0 + 8 * q;
+                    if (row < p.M && col < p.Nout)
+                        store_chunk(p.out + row * p.ld_out + col, w, p.Nout - col);
                 }
             }
+            // the accumulator is free once every lane's loads have completed
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
