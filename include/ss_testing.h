@@ -59,7 +59,9 @@ int ss_testing_s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int 
  * oracle's projections directly: out (M x Nout bf16, row stride ld_out
  * elements) = x (M x K bf16, row-major) times W (Nout x K bf16, row-major)
  * transposed, fp32 accumulation, bias[j] (fp32, device) added to columns
- * j < n_bias (bias may be null) before the one rounding to bf16.
+ * j < n_bias (bias may be null) before the one rounding to bf16. Columns
+ * from Nout up to the next multiple of 8 may be written (the output leaves
+ * as 16-byte tile stores); columns from there to ld_out are left untouched.
  * workspace: a zero-filled device block of at least 256 bytes (its header
  * takes device errors, read with ss_get_device_status). Returns
  * SS_ERR_UNSUPPORTED unless K and ld_out are multiples of 8, ld_out >= Nout

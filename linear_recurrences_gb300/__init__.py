@@ -191,8 +191,8 @@ def ss_testing_s6_describe_plan(B, L, D, N, io_dtype=SS_F32, bidir=False):
 def ss_testing_proj_gemm(x, W, bias=None, out=None, ld_out=None, workspace=None, stream=None):
     """Test hook (include/ss_testing.h): the layer's projection GEMM alone.
     x (M, K) and W (Nout, K) bf16 CUDA tensors; bias fp32 (n_bias,) added to
-    the first n_bias columns; returns out (M, ld_out) bf16 (columns >= Nout
-    untouched)."""
+    the first n_bias columns; returns out (M, ld_out) bf16 (columns from the
+    multiple of 8 at or above Nout are left untouched)."""
     torch = _torch()
     _check_cuda(x, "x", (torch.bfloat16,))
     _check_cuda(W, "W", (torch.bfloat16,))

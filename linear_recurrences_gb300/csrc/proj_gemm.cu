@@ -22,7 +22,8 @@
 //             read it and hands a finished accumulator to the epilogue;
 //   warps 2-5 epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
 //             (tile rows), 32 columns per tcgen05.ld, adds the bias, rounds
-//             to bf16 and stores 64 contiguous bytes of its row per chunk.
+//             to bf16 and writes the 32 x 32 chunk to shared memory, from
+//             where one TMA tile store sends it to global memory.
 // With two accumulators the epilogue of one tile runs under the main loop
 // of the next. CTAs run in clusters of two on neighbouring SMs: the pair
 // takes two M-blocks of the same N-block at a time, each CTA loads its own
@@ -58,10 +59,12 @@ constexpr int kThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
 constexpr int kMaxStages = 8;
 constexpr size_t kATileBytes = (size_t)kBM * kBK * 2;  // 16 KB
 constexpr size_t kSmemBudget = 224 * 1024;             // dynamic, incl. 1 KB alignment slack
+constexpr size_t kStagingBytes = 4 * 2 * 32 * 32 * 2;  // epilogue: 2 buffers of 32 x 32 bf16 per warp
 
 struct GemmParams {
     CUtensorMap tm_a;    // x as (K, M) bf16, box (64, 128), 128-byte swizzle
     CUtensorMap tm_b;    // W as (K, Nout) bf16, box (64, BN), 128-byte swizzle
+    CUtensorMap tm_out;  // out as (Nout, M) bf16, row stride ld_out, box (32, 32)
     __nv_bfloat16 *out;  // (M, ld_out) row-major
     const float *bias;   // (n_bias,) or null
     long long M;
@@ -168,18 +171,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Eight bf16 values to dst (16-byte aligned); only the first `valid` when
-// fewer than eight columns remain in the row (padding columns stay untouched).
-__device__ __forceinline__ void store_chunk(__nv_bfloat16 *dst, uint4 w, int valid) {
-    if (valid >= 8) {
-        *reinterpret_cast<uint4 *>(dst) = w;
-        return;
-    }
-    const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        if (j < valid)
-            reinterpret_cast<unsigned short *>(dst)[j] = (unsigned short)(wd[j >> 1] >> (16 * (j & 1)));
+// 2D tile copy shared -> global through a tensor map (clipped at the
+// tensor's extent), in this thread's current bulk group.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_addr(src)), "r"(x), "r"(y)
+                 : "memory");
 }
 
 // Waits for phase `parity` of `bar`; false once the CTA is aborting or the
@@ -330,11 +327,15 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         }
     } else {
         // ------------------------------------------------ epilogue
-        // Lane = tile row: each 32-column chunk leaves as four 16-byte stores
-        // per lane (64 contiguous bytes of its row). Staging the rows through
-        // shared memory to store whole row segments per instruction measured
-        // slower (it takes a pipeline stage's worth of shared memory).
+        // Lane = tile row. Each 32-column chunk is written to one of the
+        // warp's two 2 KB staging buffers in shared memory (its 32 rows x 64
+        // bytes) and leaves as one TMA tile store, clipped at M and Nout, so
+        // whole row segments reach L2 and the lanes move on while the copy
+        // runs.
         const int quarter = warp & 3;  // tensor-memory lanes 32 quarter .. + 31
+        uint4 *stg = reinterpret_cast<uint4 *>(smem + (size_t)p.stages * stage_bytes) +
+                     (size_t)(warp - 2) * 2 * 128;
+        unsigned chunk_no = 0;
         int acc = 0;
         unsigned acc_phase = 0;
         for (long long u = unit0; u < p.num_tiles; u += unit_step) {
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
             tc_fence_after();
             const long long row0 = m_block(u) * kBM + quarter * 32;
             const int n0 = (int)(u % p.n_tiles_n) * p.BN;
-            for (int c = 0; c < p.BN; c += 32) {
+            for (int c = 0; c < p.BN; c += 32, ++chunk_no) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kAccCols + c), r);
                 const int col0 = n0 + c;
@@ -358,6 +359,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] += __shfl_sync(0xffffffffu, bj, j);
                 }
+                uint4 *buf = stg + (chunk_no & 1u) * 128;
+                if (lane == 0) bulk_wait_read<1>();  // this buffer's last store has read it
+                __syncwarp();
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint4 w;
@@ -369,10 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                     w.y = *reinterpret_cast<uint32_t *>(&h1);
                     w.z = *reinterpret_cast<uint32_t *>(&h2);
                     w.w = *reinterpret_cast<uint32_t *>(&h3);
-                    const long long row = row0 + lane;
-                    const int col = col0 + 8 * q;
-                    if (row < p.M && col < p.Nout)
-                        store_chunk(p.out + row * p.ld_out + col, w, p.Nout - col);
+                    buf[lane * 4 + q] = w;
+                }
+                fence_proxy_async_smem();  // visible to the tensor copy
+                __syncwarp();
+                if (lane == 0 && row0 < p.M && col0 < p.Nout) {
+                    tma_store_2d(&p.tm_out, buf, col0, (int)row0);
+                    bulk_commit();
                 }
             }
             // the accumulator is free once every lane's loads have completed
@@ -384,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                 acc_phase ^= 1u;
             }
         }
+        if (lane == 0) bulk_wait<0>();  // every store has left shared memory
     }
     __syncthreads();
     if (warp == 1) {
@@ -415,8 +423,8 @@ GemmPlan plan_gemm(int64_t M, int64_t K, int64_t Nout) {
     g.pair = m_tiles >= 2 && (g.BN / 2) % 8 == 0;
     g.num_tiles = (g.pair ? (m_tiles + 1) / 2 : m_tiles) * g.n_tiles_n;
     const size_t stage_bytes = kATileBytes + (size_t)g.BN * kBK * 2;
-    g.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - 1024) / stage_bytes);
-    g.smem = 1024 + (size_t)g.stages * stage_bytes;
+    g.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - 1024 - kStagingBytes) / stage_bytes);
+    g.smem = 1024 + (size_t)g.stages * stage_bytes + kStagingBytes;
     return g;
 }
 
@@ -449,6 +457,13 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
         const uint64_t strides[1] = {(uint64_t)K * 2};
         const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)(g.pair ? g.BN / 2 : g.BN)};
         if (!encode_tiled_map(&prm.tm_b, W, true, 2, dims, strides, box, true))
+            return SS_ERR_UNSUPPORTED;
+    }
+    {
+        const uint64_t dims[2] = {(uint64_t)Nout, (uint64_t)M};
+        const uint64_t strides[1] = {(uint64_t)ld_out * 2};
+        const uint32_t box[2] = {32u, 32u};
+        if (!encode_tiled_map(&prm.tm_out, out, true, 2, dims, strides, box))
             return SS_ERR_UNSUPPORTED;
     }
     prm.out = static_cast<__nv_bfloat16 *>(out);
