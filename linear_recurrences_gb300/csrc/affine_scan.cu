@@ -23,10 +23,10 @@
 //    four interleaved warp-shuffle scans and a fold over the 8 warps give
 //    the tile aggregate;
 //  * the aggregate is published as two tagged 64-bit words; the control warp
-//    walks back 64 predecessors per L2 round trip (each lane loads all three
-//    words of two tiles at once) to the nearest tile that has published its
-//    inclusive state, and lane 0 applies the aggregates after it to that
-//    state one by one, in sequence order;
+//    walks back 64 predecessors per L2 round trip (each lane reads the whole
+//    32-byte descriptors of two tiles, one load each) to the nearest tile
+//    that has published its inclusive state, and lane 0 applies the
+//    aggregates after it to that state one by one, in sequence order;
 //  * the tile's inclusive state is published, and each lane re-sweeps its
 //    elements from shared memory starting at its carry-in, storing h with
 //    coalesced 128-bit streaming stores.
@@ -66,6 +66,8 @@ constexpr int kTicks = kBufs;  // tickets a CTA holds: one per buffer
 constexpr size_t kDynSmem = 2 * kBufs * kTile * sizeof(float);  // a and b per buffer
 constexpr unsigned long long kCopyTimeoutNs = 2000000000ull;  // bulk-copy completion bound
 
+// 32 bytes, 32-byte aligned (the workspace and the header are), so a poll
+// reads a whole descriptor with one load.
 struct TileDesc {
     unsigned long long agg_a;  // tag | a-part of the tile aggregate
     unsigned long long agg_b;  // tag | b-part of the tile aggregate
@@ -350,9 +352,8 @@ __device__ __forceinline__ void look_back(const AffineParams &p, unsigned tile, 
                 for (int i = 0; i < kPoll; ++i) {  // every word in flight at once
                     if (kind[i] == 0) {
                         const TileDesc *d = p.desc + (tile - 32LL * (win + 1 + i) + lane);
-                        wi[i] = ld_relaxed_u64(&d->inc);
-                        wa[i] = ld_relaxed_u64(&d->agg_a);
-                        wb[i] = ld_relaxed_u64(&d->agg_b);
+                        unsigned long long pad;
+                        ld_relaxed_u64x4(&d->agg_a, wa[i], wb[i], wi[i], pad);
                     }
                 }
                 bool pending = false;

@@ -52,6 +52,14 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// One 32-byte load (4 relaxed 64-bit words, each single-copy atomic on its
+// own); p 32-byte aligned.
+__device__ __forceinline__ void ld_relaxed_u64x4(const unsigned long long *p, unsigned long long &a,
+                                                 unsigned long long &b, unsigned long long &c,
+                                                 unsigned long long &d) {
+    asm volatile("ld.relaxed.gpu.global.v4.u64 {%0, %1, %2, %3}, [%4];"
+                 : "=l"(a), "=l"(b), "=l"(c), "=l"(d) : "l"(p) : "memory");
+}
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
