@@ -449,14 +449,14 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)M};
         const uint64_t strides[1] = {(uint64_t)K * 2};
         const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)kBM};
-        if (!encode_tiled_map(&prm.tm_a, x, true, 2, dims, strides, box, true))
+        if (!encode_tiled_map(&prm.tm_a, x, true, 2, dims, strides, box, 128))
             return SS_ERR_UNSUPPORTED;
     }
     {
         const uint64_t dims[2] = {(uint64_t)K, (uint64_t)Nout};
         const uint64_t strides[1] = {(uint64_t)K * 2};
         const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)(g.pair ? g.BN / 2 : g.BN)};
-        if (!encode_tiled_map(&prm.tm_b, W, true, 2, dims, strides, box, true))
+        if (!encode_tiled_map(&prm.tm_b, W, true, 2, dims, strides, box, 128))
             return SS_ERR_UNSUPPORTED;
     }
     {

@@ -973,7 +973,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool encode_tiled_map(void *map, const void *base, bool bf16, int rank, const uint64_t *dims,
-                      const uint64_t *strides, const uint32_t *box, bool swizzle128) {
+                      const uint64_t *strides, const uint32_t *box, int swizzle) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc || rank < 1 || rank > 5) return false;
     cuuint64_t d[5], st[4];
@@ -988,7 +988,9 @@ bool encode_tiled_map(void *map, const void *base, bool bf16, int rank, const ui
                bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+               : swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                               : CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

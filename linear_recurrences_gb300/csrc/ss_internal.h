@@ -35,12 +35,12 @@ inline int device_smem_per_sm() {
 // runtime's driver entry point) into `map` (a 128-byte CUtensorMap): `rank`
 // dimensions innermost first, dims[i] elements each, strides[i] bytes
 // between consecutive indices of dimension i + 1, box[i] elements per copy,
-// fp32 or bf16 elements, zero fill outside the extent; swizzle128: the
-// 128-byte shared-memory swizzle (the box's inner extent must be 128 bytes),
-// else none. false if the entry point is missing or the driver rejects the
-// layout.
+// fp32 or bf16 elements, zero fill outside the extent; swizzle: the
+// shared-memory swizzle span in bytes (64 or 128; the box's inner extent
+// must not exceed it), 0 for none. false if the entry point is missing or
+// the driver rejects the layout.
 bool encode_tiled_map(void *map, const void *base, bool bf16, int rank, const uint64_t *dims,
-                      const uint64_t *strides, const uint32_t *box, bool swizzle128 = false);
+                      const uint64_t *strides, const uint32_t *box, int swizzle = 0);
 
 // Projection GEMM on the tensor cores (tcgen05): out (M x Nout, row stride
 // ld_out, bf16) = x (M x K, bf16, row-major) times W (Nout x K, bf16,
