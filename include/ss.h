@@ -275,16 +275,21 @@ ss_status ss_selective_scan_fwd_state(const void *x, const void *delta,
  * proj_delta, [D, D + N) proj_B, [D + N, D + 2N) proj_C. b_delta: (D,) fp32.
  * A: (D, N) fp32 (already negative); Dskip: (D,) fp32 or NULL. proj_B and
  * proj_C carry no bias (the pages give one for proj_delta only).
- * The three projections are one dense GEMM, x times W_proj transposed, run
- * by cuBLASLt with fp32 accumulation into one (B*L) x (D + 2N) workspace
- * buffer of io_dtype (a row: pre-activation, B_t, C_t of one step); the
- * scan reads the three blocks at that row stride and applies the bias and
- * softplus itself. The workspace
- * (ss_selective_scan_layer_workspace_bytes) holds the projections, the
- * GEMM scratch and the scan's workspace (first, so ss_get_device_status
- * reads the scan's error word from it); zero it once before first use, as
- * for the scan. Errors as for ss_selective_scan_fwd; SS_ERR_UNSUPPORTED if
- * no GEMM algorithm fits the shape.
+ * The three projections are one dense GEMM, x times W_proj transposed with
+ * fp32 accumulation, into one (B*L)-row workspace buffer of io_dtype (a row:
+ * pre-activation, B_t, C_t of one step); the scan reads the three blocks at
+ * that row stride and applies softplus itself. As a Linear layer with a
+ * bias, the pre-activation is the product plus b_delta rounded once to
+ * io_dtype: for SS_BF16 the library's tensor-core GEMM adds the bias to the
+ * fp32 accumulator before the one rounding to bf16 (D must be a multiple of
+ * 8, x and W_proj 16-byte aligned, else SS_ERR_UNSUPPORTED); for SS_F32 a
+ * cuBLASLt fp32 GEMM writes the product and the scan adds the bias in fp32.
+ * The workspace (ss_selective_scan_layer_workspace_bytes) holds the
+ * projections, any GEMM scratch and the scan's workspace (first, so
+ * ss_get_device_status reads the error word from it: the scan's, and the
+ * GEMM's for a wait that ran out); zero it once before first use, as for the
+ * scan. Errors as for ss_selective_scan_fwd; SS_ERR_UNSUPPORTED also if no
+ * GEMM algorithm fits the shape.
  */
 size_t ss_selective_scan_layer_workspace_bytes(int64_t B, int64_t L, int64_t D,
                                                int64_t N, int io_dtype);
