@@ -101,6 +101,13 @@ __host__ __device__ inline WSSmem ws_smem(int R, int S, int es, int wc) {
 
 __device__ __forceinline__ float ld_smem_io(const float *p) { return *p; }
 __device__ __forceinline__ float ld_smem_io(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+// Two adjacent values (p aligned to two elements), widened to fp32.
+__device__ __forceinline__ float2 ld_smem_io2(const float *p) {
+    return *reinterpret_cast<const float2 *>(p);
+}
+__device__ __forceinline__ float2 ld_smem_io2(const __nv_bfloat16 *p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
+}
 
 // 12 resident warps per SM (170 registers a thread): three four-warp CTAs.
 template <typename IO, int T, int S>
@@ -195,6 +202,20 @@ __global__ void __launch_bounds__(S * 32, 12 / S) s6_ws_kernel(const __grid_cons
 
     const float Dd = dsk[c];
     const float dbias = dbs[c];
+    // this lane's share of the B_t / C_t widening (the same every block):
+    // entries it = c + 32 w of wbc, each from rows r, r + 1 (r = 2 ip) and
+    // states 2k, 2k + 1 of tile m
+    constexpr int kWiden = (2 * kPairs * P2 + 31) / 32;
+    int wsrc[kWiden];
+    bool wtwo[kWiden], wok[kWiden];
+#pragma unroll
+    for (int w = 0; w < kWiden; ++w) {
+        const int it = c + 32 * w;
+        const int ip = it % P2, k = (it / P2) % kPairs, m = it / (P2 * kPairs);
+        wok[w] = it < 2 * kPairs * P2;
+        wtwo[w] = 2 * ip + 1 < T;
+        wsrc[w] = m * (L_.bt / (int)sizeof(IO)) + 2 * ip * 16 + 2 * k;
+    }
     const bool sp = p.softplus != 0;
     const int row0 = s * T;                                               // this slice's first row
     float4 *wbc = reinterpret_cast<float4 *>(sm + L_.off_bc + s * WC);   // this warp's B_t / C_t
@@ -235,14 +256,13 @@ __global__ void __launch_bounds__(S * 32, 12 / S) s6_ws_kernel(const __grid_cons
             // widen this slice's rows into wbc[(m*kPairs + k)*P2 + ip] =
             // {M[r][2k], M[r][2k+1], M[r+1][2k], M[r+1][2k+1]}, r = 2*ip
             const IO *bs = reinterpret_cast<const IO *>(sm + L_.off_bs + st * 2 * L_.bt) + row0 * 16;
-            constexpr int items = 2 * kPairs * P2;
-            for (int it = c; it < items; it += 32) {
-                const int ip = it % P2, k = (it / P2) % kPairs, m = it / (P2 * kPairs);
-                const IO *M = bs + m * (L_.bt / (int)sizeof(IO)) + 2 * ip * 16 + 2 * k;
-                const bool two = 2 * ip + 1 < T;
-                wbc[it] = make_float4(ld_smem_io(M), ld_smem_io(M + 1),
-                                      two ? ld_smem_io(M + 16) : 0.0f,
-                                      two ? ld_smem_io(M + 17) : 0.0f);
+#pragma unroll
+            for (int w = 0; w < kWiden; ++w) {
+                if (!wok[w]) continue;
+                const IO *M = bs + wsrc[w];
+                const float2 r0 = ld_smem_io2(M);
+                const float2 r1 = wtwo[w] ? ld_smem_io2(M + 16) : make_float2(0.0f, 0.0f);
+                wbc[c + 32 * w] = make_float4(r0.x, r0.y, r1.x, r1.y);
             }
             __syncwarp();
         }
