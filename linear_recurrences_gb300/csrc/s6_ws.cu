@@ -39,6 +39,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 
 #include "f32x2.cuh"
 #include "s6_common.cuh"
@@ -69,7 +70,7 @@ struct WSParams {
     float *h_last;
     WsHeader *ws;
     long long L, D;
-    int N, nblk, dgroups, softplus;
+    int N, nblk, dgroups;
     unsigned long long timeout_ns;
 };
 
@@ -110,7 +111,7 @@ __device__ __forceinline__ float2 ld_smem_io2(const __nv_bfloat16 *p) {
 }
 
 // 12 resident warps per SM (170 registers a thread): three four-warp CTAs.
-template <typename IO, int T, int S>
+template <typename IO, int T, int S, bool SP>
 __global__ void __launch_bounds__(S * 32, 12 / S) s6_ws_kernel(const __grid_constant__ WSParams p) {
     static_assert(S >= 2, "the hand-off needs two warps or more");
     using C = WSShape<T, S>;
@@ -216,7 +217,6 @@ __global__ void __launch_bounds__(S * 32, 12 / S) s6_ws_kernel(const __grid_cons
         wtwo[w] = 2 * ip + 1 < T;
         wsrc[w] = m * (L_.bt / (int)sizeof(IO)) + 2 * ip * 16 + 2 * k;
     }
-    const bool sp = p.softplus != 0;
     const int row0 = s * T;                                               // this slice's first row
     float4 *wbc = reinterpret_cast<float4 *>(sm + L_.off_bc + s * WC);   // this warp's B_t / C_t
     u64 ddl[T], uu[T], yv[T];
@@ -239,17 +239,23 @@ __global__ void __launch_bounds__(S * 32, 12 / S) s6_ws_kernel(const __grid_cons
             const IO *xt = reinterpret_cast<const IO *>(sm + st * L_.xt) + row0 * kCH + c;
             const IO *dt = reinterpret_cast<const IO *>(sm + L_.off_d + st * L_.xt) + row0 * kCH + c;
             const long long lim = L - (long long)j * R - row0;  // steps of this slice inside L
+            auto enter = [&](auto whole) {
 #pragma unroll
-            for (int i = 0; i < T; ++i) {
-                float dv = ld_smem_io(dt + i * kCH) + dbias;
-                if (sp) dv = softplus_mufu(dv);
-                if (i >= lim) dv = 0.0f;  // past L: dA = 1, no input
-                const float xv = ld_smem_io(xt + i * kCH);
-                const float u = dv * xv;
-                ddl[i] = f2(dv, dv);
-                uu[i] = f2(u, u);
-                yv[i] = f2(Dd * xv, 0.0f);
-            }
+                for (int i = 0; i < T; ++i) {
+                    float dv = ld_smem_io(dt + i * kCH) + dbias;
+                    if constexpr (SP) dv = softplus_mufu(dv);
+                    if (!decltype(whole)::value && i >= lim) dv = 0.0f;  // past L: dA = 1, no input
+                    const float xv = ld_smem_io(xt + i * kCH);
+                    const float u = dv * xv;
+                    ddl[i] = f2(dv, dv);
+                    uu[i] = f2(u, u);
+                    yv[i] = f2(Dd * xv, 0.0f);
+                }
+            };
+            if (lim >= T)
+                enter(std::true_type{});  // every block but possibly the last
+            else
+                enter(std::false_type{});
         }
         wait(bbar + st, (unsigned)(j / kNX) & 1u, 10u);
         {
@@ -400,9 +406,8 @@ ss_status launch_shape(const S6Args &a, const WSPlan &pl, void *workspace, cudaS
     prm.N = (int)a.N;
     prm.nblk = pl.nblk;
     prm.dgroups = pl.dgroups;
-    prm.softplus = a.softplus;
     prm.timeout_ns = timeout_ns;
-    auto kern = s6_ws_kernel<IO, T, S>;
+    auto kern = a.softplus ? s6_ws_kernel<IO, T, S, true> : s6_ws_kernel<IO, T, S, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
         cudaSuccess)
         return SS_ERR_CUDA;
