@@ -419,6 +419,44 @@ def bench_proj_gemm(torch, ss, dev, steps, warmup, stream):
             "l2": "inputs (100 MB x + 4.8 MB W) near L2 size, no flush"}
 
 
+def round_floats(v, digits=5):
+    """The JSON line with floats at `digits` significant digits (the timing
+    noise is larger), so the line stays short enough to read whole."""
+    if isinstance(v, float):
+        return float(f"{v:.{digits}g}")
+    if isinstance(v, dict):
+        return {k: round_floats(x, digits) for k, x in v.items()}
+    if isinstance(v, list):
+        return [round_floats(x, digits) for x in v]
+    return v
+
+
+def config_summary(per_cfg, line):
+    """One short entry per workload, the five configurations of the problem
+    last: time per call, fraction of its roofline, and the oracle's rate on
+    one thread and on every core (elements/s) beside the GPU's."""
+    order = ["proj_gemm_bf16", "affine_large_log_step", "s6_bf16_state", "s6_fp32_bwd",
+             "s6_bf16_bwd", "s6_bf16_layer", "affine_small_graph",
+             "affine_small", "affine_large", "s6_fp32", "s6_bf16", "s6_bidir"]
+    out = {}
+    for name in order:
+        e = per_cfg.get(name)
+        if not e:
+            continue
+        r = {"ms": e.get("ms")}
+        if e.get("roofline_frac") is not None:
+            r["roofline_frac"] = e["roofline_frac"]
+        if e.get("elements_per_s") is not None:
+            r["elem_per_s"] = e["elements_per_s"]
+        cb = e.get("cpu_baseline") or (line.get("cpu_baseline") if name == "affine_large" else None)
+        if cb:
+            r["oracle_elem_per_s"] = {"1_thread": cb.get("value_1_thread", cb["value"] if cb.get("cores") == 1 else None),
+                                      "all_cores": cb["value"] if cb.get("cores", 1) > 1 else None,
+                                      "cores": cb.get("host_cores", cb.get("cores"))}
+        out[name] = r
+    return out
+
+
 # ---------------------------------------------------------------- arms
 def run_reference(args, rank):
     if rank != 0:
@@ -637,7 +675,9 @@ def run_ours(args, rank, world, local_rank):
         "source_hash": src,
     }
     line.update(extras)
-    print(json.dumps(line), flush=True)
+    if "per_config" in extras:
+        line["summary"] = config_summary(extras["per_config"], line)
+    print(json.dumps(round_floats(line)), flush=True)
 
 
 def run_single(args):

@@ -54,3 +54,21 @@ def test_reference_arm_nonzero_rank_exits_without_work():
                        timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_summary_puts_the_five_configurations_last():
+    """The JSON line ends with a short per-workload summary whose last five
+    entries are the problem's five configurations (the part of a long line a
+    tail shows)."""
+    import bench
+    per = {n: {"ms": 1.0, "roofline_frac": 0.5, "elements_per_s": 2.0}
+           for n in ("s6_bidir", "affine_small", "s6_fp32_bwd", "affine_large", "s6_fp32",
+                     "s6_bf16", "s6_bf16_layer")}
+    per["s6_fp32"]["cpu_baseline"] = {"value": 8.0, "value_1_thread": 1.0, "cores": 16,
+                                      "host_cores": 16}
+    out = bench.config_summary(per, {"cpu_baseline": {"value": 3.0, "cores": 1, "host_cores": 16}})
+    assert list(out)[-5:] == ["affine_small", "affine_large", "s6_fp32", "s6_bf16", "s6_bidir"]
+    assert out["s6_fp32"]["oracle_elem_per_s"] == {"1_thread": 1.0, "all_cores": 8.0, "cores": 16}
+    assert out["affine_large"]["oracle_elem_per_s"]["1_thread"] == 3.0
+    r = bench.round_floats({"a": 1.23456789, "b": [7, 2.0000001], "c": "x"})
+    assert r == {"a": 1.2346, "b": [7, 2.0], "c": "x"}
