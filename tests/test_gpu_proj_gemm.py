@@ -27,15 +27,14 @@ def ss():
 
 
 def gemm_case(M, K, Nout, n_bias, seed):
-    """x (M, K), W (Nout, K), bias (n_bias,) on the exact-sum grid."""
-    Dq = max(K, 1)
-    x, W, b, _, _ = workloads.layer_inputs(1, M, K, 0, io="bf16", seed=seed)
-    g = workloads.generator(seed + 1)
-    Wn = g.standard_normal((Nout, K)) / np.sqrt(Dq)
-    Wn = workloads.bf16_bits_to_f32(workloads.f32_to_bf16_bits(Wn.astype(np.float32)))
-    Wn[np.abs(Wn) < 2.0 ** -8] = 0.0
-    bias = np.round(g.normal(-4.0, 1.0, n_bias) * 2.0 ** 20) / 2.0 ** 20
-    return x.reshape(M, K), Wn, bias.astype(np.float32)
+    """x (M, K) ~ N(0, 1), W (Nout, K) ~ N(0, 1/K), bias (n_bias,) ~ N(-4, 1),
+    on the exact-sum grid."""
+    g = workloads.generator(seed)
+    x = g.standard_normal((M, K))
+    W = g.standard_normal((Nout, K)) / np.sqrt(max(K, 1))
+    b = g.normal(-4.0, 1.0, n_bias)
+    x, W, b = workloads.exact_sum_grid(x, W, b)
+    return x.astype(np.float32), W.astype(np.float32), b.astype(np.float32)
 
 
 def run(ss, torch, x, W, bias, ld_out=None, sentinel=None):

@@ -197,9 +197,19 @@ def layer_inputs(B: int, L: int, D: int, N: int, *, io: str = "f32", seed: int =
     A = -g.uniform(0.1, 4.0, (D, N))
     Ds = g.standard_normal(D)
     if io == "bf16":
-        x = np.clip(np.round(x * 32.0), -127, 127) / 32.0
-        W = bf16_bits_to_f32(f32_to_bf16_bits(W.astype(np.float32))).astype(np.float64)
-        W[np.abs(W) < 2.0 ** -8] = 0.0
-        b = np.round(b * 2.0 ** 20) / 2.0 ** 20
+        x, W, b = exact_sum_grid(x, W, b)
     f = lambda v: np.ascontiguousarray(v, dtype=np.float32)
     return f(x), f(W), f(b), f(A), f(Ds)
+
+
+def exact_sum_grid(x, W, b):
+    """Puts GEMM operands on the grid on which x W^T + b is exact in fp32 in
+    any summation order (for |x W^T + b| < 16): x on multiples of 2^-5 inside
+    (-4, 4), W rounded to bf16 with magnitudes below 2^-8 set to 0 (every
+    product a multiple of 2^-20), b on multiples of 2^-20. x and W are then
+    bf16 values. Returns float64 arrays."""
+    x = np.clip(np.round(np.asarray(x, np.float64) * 32.0), -127, 127) / 32.0
+    W = bf16_bits_to_f32(f32_to_bf16_bits(np.asarray(W, np.float32))).astype(np.float64)
+    W[np.abs(W) < 2.0 ** -8] = 0.0
+    b = np.round(np.asarray(b, np.float64) * 2.0 ** 20) / 2.0 ** 20
+    return x, W, b
