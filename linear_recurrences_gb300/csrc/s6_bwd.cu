@@ -33,7 +33,6 @@
 
 #include <algorithm>
 #include <cstdint>
-#include <cstdlib>
 
 #include "f32x2.cuh"
 #include "s6_common.cuh"
@@ -637,10 +636,6 @@ BwdPlan bwd_plan(int64_t B, int64_t L, int64_t D, int64_t N) {
             best_cost = cost;
             best_Dr = Dr;
         }
-    }
-    if (const char *e = std::getenv("SS_BWD_SD")) {  // tuning override: channel ranges
-        const long long sd = std::atoll(e);
-        if (sd >= 1 && sd <= groups) best_Dr = (groups + sd - 1) / sd * kWarps;
     }
     pl.Dr = (int)best_Dr;
     pl.SD = (int)((D + pl.Dr - 1) / pl.Dr);
