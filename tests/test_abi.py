@@ -159,6 +159,17 @@ def test_product_path_never_touches_the_oracle():
                 assert "oracle" not in text.lower(), f"{f} mentions the oracle"
 
 
+def test_library_reads_no_environment():
+    """Plans and workspace sizes depend on the call's arguments only: no
+    source of the library reads an environment variable (a stray one could
+    change a plan between a workspace-size query and the launch)."""
+    csrc = os.path.join(ROOT, "linear_recurrences_gb300", "csrc")
+    for f in os.listdir(csrc):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            text = open(os.path.join(csrc, f)).read()
+            assert "getenv" not in text and "environ" not in text, f"{f} reads the environment"
+
+
 def _chunked_plan(B, Lq, D, N, io, bidir):
     """(chunks per sequence, warps per CTA, timesteps per warp) the chunked
     kernel's planner takes for a shape (the time-parallel pass set aside)."""
