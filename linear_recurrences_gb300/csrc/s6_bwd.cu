@@ -29,6 +29,7 @@
 //   4. fixed-order sums: dB, dC over the channel ranges; dA, dD over (b,
 //      chunk).
 // Every reduction has a fixed order, so results are bitwise reproducible.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -63,6 +64,9 @@ struct BwdParams {
     int Dr;          // channels per range (multiple of kWarps)
     int softplus;
     int vec_rows;    // x, delta, dy, dx, ddelta 16-byte aligned with 16-byte rows
+    int tma_rows;    // tm_x, tm_d, tm_dy hold valid tensor maps (aggregate launch)
+    unsigned long long timeout_ns;
+    CUtensorMap tm_x, tm_d, tm_dy;  // 3D (D, L, B) maps, box (32, kAggStage, 1)
     // workspace, each [B][K][D][N] unless noted
     float *aggP, *aggH, *aggM;   // chunk aggregates
     float *carH, *carM;          // state entering / adjoint leaving each chunk
@@ -304,12 +308,20 @@ __device__ __forceinline__ void read_items(const BwdParams &p, const ChunkCtx &c
 // in time order: (P, H, M) then (P', H', M') = (P P', P' H + H', M + P M').
 constexpr int kAggWarps = 4;
 constexpr int kAggSteps = kChunk / kAggWarps;  // steps per warp
-constexpr int kAggSmem =
-    (2 * kChunk * kMaxN + 3 * (kAggWarps - 1) * 32 * kMaxN) * (int)sizeof(float);  // 38 KB
+constexpr int kAggStage = 32;                  // steps per staged tile of x, delta, dy
+constexpr int kAggSmemBase =
+    (2 * kChunk * kMaxN + 3 * (kAggWarps - 1) * 32 * kMaxN) * (int)sizeof(float);  // 50 KB
+// plus, per warp, one staged tile of x, delta and dy (kAggStage rows of 32
+// channels each) and its mbarrier
+template <typename IO>
+constexpr int agg_smem() {
+    return kAggSmemBase + kAggWarps * (3 * kAggStage * 32 * (int)sizeof(IO) + 16);
+}
 
 template <typename IO>
-__global__ void __launch_bounds__(32 * kAggWarps, 4) bwd_aggregate_kernel(const BwdParams p) {
-    extern __shared__ __align__(16) float smem[];  // kAggSmem bytes
+__global__ void __launch_bounds__(32 * kAggWarps, 4)
+bwd_aggregate_kernel(const __grid_constant__ BwdParams p) {
+    extern __shared__ __align__(128) float smem[];  // agg_smem<IO>() bytes
     float *sB = smem, *sC = smem + kChunk * kMaxN;  // [step][16], zeros past N and L
     u64 *fold = reinterpret_cast<u64 *>(sC + kChunk * kMaxN);  // [warp-1][P, H, M][pair][lane]
     const long long groups = (p.D + 31) / 32;
@@ -343,15 +355,47 @@ __global__ void __launch_bounds__(32 * kAggWarps, 4) bwd_aggregate_kernel(const 
         P[q] = kOne2;
         H[q] = M[q] = 0ull;
     }
+    // this warp's staged tiles: [x | delta | dy][kAggStage rows][32 channels]
+    IO *stile = reinterpret_cast<IO *>(reinterpret_cast<unsigned char *>(smem) + kAggSmemBase) +
+                warp * 3 * kAggStage * 32;
+    uint64_t *sbar = reinterpret_cast<uint64_t *>(
+        reinterpret_cast<unsigned char *>(smem) + kAggSmemBase +
+        kAggWarps * 3 * kAggStage * 32 * (int)sizeof(IO)) + warp;
+    if (p.tma_rows && lane == 0) {
+        mbar_init(sbar, 1);
+        fence_mbar_init();
+    }
     __syncthreads();  // the Bt, Ct rows are in place
     const IO *xp = static_cast<const IO *>(p.x);
     const IO *dp = static_cast<const IO *>(p.delta);
     const IO *yp = static_cast<const IO *>(p.dy);
     const int s0 = warp * kAggSteps, s1 = min(steps, s0 + kAggSteps);
+    const int d0 = (int)((blockIdx.x % groups) * 32);
+    unsigned use = 0;  // staged tiles consumed (the barrier's phase)
 #pragma unroll 4
     for (int tl = s0; tl < s1; ++tl) {
         float v = 0.0f, x = 0.0f, gy = 0.0f;
-        if (dok) {
+        if (p.tma_rows) {
+            // rows of x, delta, dy of the next kAggStage steps: three tile
+            // copies issued at once by one lane (zero-filled past D and L)
+            const int r = (tl - s0) % kAggStage;
+            if (r == 0) {
+                __syncwarp();  // every lane is done with the previous tile
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(sbar, 3u * kAggStage * 32 * (unsigned)sizeof(IO));
+                    const int ty = (int)(t0 + tl);
+                    tma_load_3d(stile, &p.tm_x, d0, ty, (int)b, sbar);
+                    tma_load_3d(stile + kAggStage * 32, &p.tm_d, d0, ty, (int)b, sbar);
+                    tma_load_3d(stile + 2 * kAggStage * 32, &p.tm_dy, d0, ty, (int)b, sbar);
+                }
+                mbar_wait_bounded(sbar, use & 1u, p.timeout_ns);
+                ++use;
+            }
+            x = to_f32(stile[r * 32 + lane]);
+            v = to_f32(stile[(kAggStage + r) * 32 + lane]);
+            gy = to_f32(stile[(2 * kAggStage + r) * 32 + lane]);
+        } else if (dok) {
             const long long g = (b * p.L + t0 + tl) * p.D + d;
             v = ld_io(dp, g);
             x = ld_io(xp, g);
@@ -456,7 +500,7 @@ constexpr int kGradSmem =
 // written once at the end.
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) bwd_grad_kernel(const BwdParams p) {
-    extern __shared__ __align__(16) float smem[];  // kGradSmem bytes
+    extern __shared__ __align__(128) float smem[];  // kGradSmem bytes
     float *Bs = smem, *Cs = Bs + kMaxN * kChunk;
     float *accB = Cs + kMaxN * kChunk, *accC = accB + kMaxN * kChunk;  // [n][item][lane]
     float *redB = accC + kMaxN * kChunk, *redC = redB + kWarps * kChunk;  // [warp][item][lane]
@@ -696,6 +740,14 @@ ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cu
                                reinterpret_cast<uintptr_t>(a.dy) | reinterpret_cast<uintptr_t>(a.dx) |
                                reinterpret_cast<uintptr_t>(a.ddelta);
         p.vec_rows = (ptrs & 15u) == 0 && ((uintptr_t)a.D * es) % 16 == 0;
+        p.timeout_ns = spin_timeout_ns();
+        const uint64_t dims[3] = {(uint64_t)a.D, (uint64_t)a.L, (uint64_t)a.B};
+        const uint64_t strides[2] = {(uint64_t)a.D * es, (uint64_t)(a.L * a.D) * es};
+        const uint32_t box[3] = {32u, (uint32_t)kAggStage, 1u};
+        const bool bf = a.io_bf16 != 0;
+        p.tma_rows = p.vec_rows && encode_tiled_map(&p.tm_x, a.x, bf, 3, dims, strides, box) &&
+                     encode_tiled_map(&p.tm_d, a.delta, bf, 3, dims, strides, box) &&
+                     encode_tiled_map(&p.tm_dy, a.dy, bf, 3, dims, strides, box);
     }
     char *ws = static_cast<char *>(workspace);
     float **sec[9] = {&p.aggP, &p.aggH, &p.aggM, &p.carH, &p.carM, &p.partA, &p.partD, &p.partB, &p.partC};
@@ -705,10 +757,11 @@ ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cu
     const long long agg_grid = a.B * pl.K * ((a.D + 31) / 32);
     if (agg_grid > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
     auto agg = a.io_bf16 ? bwd_aggregate_kernel<__nv_bfloat16> : bwd_aggregate_kernel<float>;
-    if (cudaFuncSetAttribute(agg, cudaFuncAttributeMaxDynamicSharedMemorySize, kAggSmem) !=
+    const int agg_smem_bytes = a.io_bf16 ? agg_smem<__nv_bfloat16>() : agg_smem<float>();
+    if (cudaFuncSetAttribute(agg, cudaFuncAttributeMaxDynamicSharedMemorySize, agg_smem_bytes) !=
         cudaSuccess)
         return SS_ERR_CUDA;
-    agg<<<(unsigned)agg_grid, 32 * kAggWarps, kAggSmem, stream>>>(p);
+    agg<<<(unsigned)agg_grid, 32 * kAggWarps, agg_smem_bytes, stream>>>(p);
     const long long chains = a.B * a.D * a.N;
     bwd_carry_kernel<<<(unsigned)((chains + 255) / 256), 256, 0, stream>>>(p);
     auto grad = a.io_bf16 ? bwd_grad_kernel<__nv_bfloat16> : bwd_grad_kernel<float>;
