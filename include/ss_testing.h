@@ -35,7 +35,7 @@ void ss_testing_skip_publish_once(int64_t unit);
  * per warp, `b` steps per lane and `c` warps per CTA (built variants: a in
  * {2, 4, 8}, b in {7, 9}); kind 3: the wavefront single pass with `a` steps
  * per warp slice and `b` slices (warps) per CTA (built: (9, 4), (11, 4),
- * (13, 4), (9, 2), (13, 2)). Kinds 2 and 3 apply to forward calls only (else the
+ * (13, 4), (15, 4), (9, 2), (13, 2)). Kinds 2 and 3 apply to forward calls only (else the
  * planner's choice applies). A workspace sized under one setting is only valid under that
  * setting; calls made while another thread changes it may take either.
  */

@@ -416,7 +416,7 @@ ss_status launch_shape(const S6Args &a, const WSPlan &pl, void *workspace, cudaS
 }
 
 // Every built (T, S) variant.
-#define WS_VARIANTS(X) X(9, 4) X(11, 4) X(13, 4) X(9, 2) X(13, 2)
+#define WS_VARIANTS(X) X(9, 4) X(11, 4) X(13, 4) X(15, 4) X(9, 2) X(13, 2)
 
 template <typename IO>
 ss_status launch_io(const S6Args &a, const WSPlan &pl, void *ws, cudaStream_t st,
@@ -460,10 +460,11 @@ bool ws_make_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int T
 bool ws_choose_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_bf16, int sms,
                     WSPlan *out) {
     // Every CTA walks all of L, so the shape needs channels for two CTAs
-    // per SM (32 channels each) or more; 11 steps per slice and 4 slices
-    // measured fastest on the bf16 forward workload (9 and 13: 1-4% slower).
+    // per SM (32 channels each) or more; 13 steps per slice and 4 slices
+    // measured fastest on the bf16 forward workload (11: 4% slower, 15:
+    // equal, 9 and 17: 5-10% slower).
     WSPlan pl{};
-    if (N > 16 || !ws_make_plan(B, L, D, N, io_bf16, 11, 4, &pl)) return false;
+    if (N > 16 || !ws_make_plan(B, L, D, N, io_bf16, 13, 4, &pl)) return false;
     if (pl.ctas < 2LL * sms) return false;
     *out = pl;
     return true;

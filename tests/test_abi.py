@@ -201,10 +201,10 @@ def test_planner_paths(L):
     assert ss.ss_testing_s6_describe_plan(2, 16384, 768, 16, ss.SS_F32, 1)[0] == 0
     assert ss.ss_testing_s6_describe_plan(1, 5000, 64, 16, ss.SS_F32, 0)[0] == 0
     # forward shapes with channels for two 32-channel CTAs per SM: the
-    # wavefront single pass (11 steps x 4 slices); the fp32 workload has 128
+    # wavefront single pass (13 steps x 4 slices); the fp32 workload has 128
     # such CTAs and stays chunked
     assert ss.ss_testing_s6_describe_plan(8, 4096, 1536, 16, ss.SS_BF16, 0) == \
-        (2, (11, 4, 32, 94, 384, 44))
+        (2, (13, 4, 32, 79, 384, 52))
     assert ss.ss_testing_s6_describe_plan(16, 2048, 256, 16, ss.SS_F32, 0)[0] == 0
     ss.ss_testing_s6_plan(2, 4, 9, 2)
     try:

@@ -15,7 +15,7 @@ TOL_STATE = {"f32": 1e-4, "bf16": 1e-3}
 THREADS = os.cpu_count() or 1
 
 # (steps per warp slice T, slices per CTA S); a block is S * T steps of 32 channels
-VARIANTS = [(9, 4), (11, 4), (13, 4), (9, 2), (13, 2)]
+VARIANTS = [(9, 4), (11, 4), (13, 4), (15, 4), (9, 2), (13, 2)]
 
 
 @pytest.fixture(scope="module")
@@ -102,11 +102,11 @@ def test_variant_parity(torch, ss, ws_plan, shape, variant, io, softplus):
 def test_workload_every_element(torch, ss, ws_plan, name):
     """The fp32 and bf16 forward workloads at full size through the wavefront
     pass: every output element against the oracle."""
-    ws_plan(11, 4)
+    ws_plan(13, 4)
     w = workloads.S6[name]
     io = ss.SS_BF16 if w.io == "bf16" else ss.SS_F32
     kind, prm = ss.ss_testing_s6_describe_plan(w.B, w.L, w.D, w.N, io)
-    assert kind == 2 and prm[:2] == (11, 4)
+    assert kind == 2 and prm[:2] == (13, 4)
     inp = workloads.s6_workload_inputs(w)
     dev = torch.device("cuda:0")
     t = lambda v: to_dev(v, dev, inp.io)
