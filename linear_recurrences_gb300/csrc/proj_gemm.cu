@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "ss_common.cuh"
 #include "ss_internal.h"
@@ -428,6 +429,64 @@ GemmPlan plan_gemm(int64_t M, int64_t K, int64_t Nout) {
     return g;
 }
 
+// Per device: the SM count and the pairs that fit at once for the last
+// shared-memory size asked for, and the kernels' dynamic shared-memory limit
+// (a per-device attribute, only ever raised, so a launch sized under an
+// earlier query stays valid). Filled on first use and when the size
+// changes, under a lock.
+struct LaunchInfo {
+    int smem = -1, sms = 0, clusters = 0, smem_limit = 0;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_info_mutex;
+LaunchInfo g_info[kMaxDevices];
+
+ss_status launch_info(size_t smem, LaunchInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SS_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SS_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_info_mutex);
+    LaunchInfo &li = g_info[dev];
+    if (li.smem != (int)smem) {
+        int sms = 0, clusters = 0;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const int limit = std::max(li.smem_limit, (int)smem);
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms < 2 ||
+            cudaFuncSetAttribute(proj_gemm_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(proj_gemm_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, limit) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return SS_ERR_CUDA;
+        }
+        li.smem_limit = limit;
+        cfg.gridDim = dim3(2 * (unsigned)(sms / 2), 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&clusters, proj_gemm_kernel<true>, &cfg) !=
+                cudaSuccess ||
+            clusters < 1) {
+            cudaGetLastError();
+            return SS_ERR_CUDA;
+        }
+        li.smem = (int)smem;
+        li.sms = sms;
+        li.clusters = clusters;
+    }
+    *out = li;
+    return SS_OK;
+}
+
 }  // namespace
 
 bool proj_gemm_supported(const void *x, const void *W, const void *out, int64_t M, int64_t K,
@@ -485,18 +544,14 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
     // 17-22, M >> 4 in bits 24-28
     prm.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((unsigned)(g.BN >> 3) << 17) |
                 ((unsigned)(kBM >> 4) << 24);
+    LaunchInfo li;
+    const ss_status st = launch_info(g.smem, &li);
+    if (st != SS_OK) return st;
     if (!g.pair) {
-        if (cudaFuncSetAttribute(proj_gemm_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)g.smem) != cudaSuccess)
-            return SS_ERR_CUDA;
-        const long long grid = std::min<long long>(g.num_tiles, device_sm_count());
+        const long long grid = std::min<long long>(g.num_tiles, li.sms);
         proj_gemm_kernel<false><<<(unsigned)grid, kThreads, g.smem, stream>>>(prm);
         return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
     }
-    if (cudaFuncSetAttribute(proj_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)g.smem) != cudaSuccess)
-        return SS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -508,16 +563,8 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // as many pairs as can be resident at once (all CTAs of a persistent
-    // grid run together), capped by the work
-    int clusters = 0;
-    cfg.gridDim = dim3(2 * (unsigned)std::max(1, device_sm_count() / 2), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&clusters, proj_gemm_kernel<true>, &cfg) != cudaSuccess ||
-        clusters < 1) {
-        cudaGetLastError();
-        return SS_ERR_CUDA;
-    }
-    cfg.gridDim = dim3(2 * (unsigned)std::min<long long>(g.num_tiles, clusters), 1, 1);
+    // as many pairs as can be resident at once, capped by the work
+    cfg.gridDim = dim3(2 * (unsigned)std::min<long long>(g.num_tiles, li.clusters), 1, 1);
     if (cudaLaunchKernelEx(&cfg, proj_gemm_kernel<true>, prm) != cudaSuccess) return SS_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }

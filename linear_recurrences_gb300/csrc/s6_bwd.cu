@@ -758,15 +758,13 @@ ss_status s6_bwd_launch(const S6BwdArgs &a, void *workspace, size_t ws_bytes, cu
     if (agg_grid > 0x7fffffffLL) return SS_ERR_UNSUPPORTED;
     auto agg = a.io_bf16 ? bwd_aggregate_kernel<__nv_bfloat16> : bwd_aggregate_kernel<float>;
     const int agg_smem_bytes = a.io_bf16 ? agg_smem<__nv_bfloat16>() : agg_smem<float>();
-    if (cudaFuncSetAttribute(agg, cudaFuncAttributeMaxDynamicSharedMemorySize, agg_smem_bytes) !=
-        cudaSuccess)
+    if (raise_smem_limit(reinterpret_cast<const void *>(agg), agg_smem_bytes) != SS_OK)
         return SS_ERR_CUDA;
     agg<<<(unsigned)agg_grid, 32 * kAggWarps, agg_smem_bytes, stream>>>(p);
     const long long chains = a.B * a.D * a.N;
     bwd_carry_kernel<<<(unsigned)((chains + 255) / 256), 256, 0, stream>>>(p);
     auto grad = a.io_bf16 ? bwd_grad_kernel<__nv_bfloat16> : bwd_grad_kernel<float>;
-    if (cudaFuncSetAttribute(grad, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradSmem) !=
-        cudaSuccess)
+    if (raise_smem_limit(reinterpret_cast<const void *>(grad), kGradSmem) != SS_OK)
         return SS_ERR_CUDA;
     grad<<<(unsigned)grid, kThreads, kGradSmem, stream>>>(p);
     bwd_final_kernel<<<device_sm_count() * 8, 256, 0, stream>>>(p);

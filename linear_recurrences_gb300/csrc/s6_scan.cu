@@ -914,11 +914,9 @@ bool encode_2d(CUtensorMap *m, const void *base, bool bf16, uint64_t inner, uint
 template <int NG, int LPC, typename IO, bool SP, bool BIDIR>
 ss_status launch_t(const S6Params &prm, const Plan &pl, cudaStream_t stream) {
     auto kern = s6_kernel<NG, LPC, IO, SP, BIDIR>;
-    if (pl.smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
-            cudaSuccess)
-            return SS_ERR_CUDA;
-    }
+    if (pl.smem > 48 * 1024 &&
+        raise_smem_limit(reinterpret_cast<const void *>(kern), (int)pl.smem) != SS_OK)
+        return SS_ERR_CUDA;
     if (BIDIR && pl.K > 1) {
         // every chunk of one sequence must be resident at the same time
         int per_sm = 0;

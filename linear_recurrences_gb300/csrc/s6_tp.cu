@@ -504,8 +504,7 @@ ss_status launch_shape(const S6Args &a, const TPPlan &pl, void *workspace, size_
 
     // 2) the scan, launched as a programmatic dependent of the packing kernel
     auto kern = s6_tp_kernel<IO, G, T, W>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
-        cudaSuccess)
+    if (raise_smem_limit(reinterpret_cast<const void *>(kern), (int)pl.smem) != SS_OK)
         return SS_ERR_CUDA;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)pl.ctas);
@@ -588,8 +587,7 @@ int tp_ctas_per_sm(const TPPlan &pl, int io_bf16) {
 #undef TP_FN
     int n = 0;
     if (!fn ||
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
-            cudaSuccess ||
+        raise_smem_limit(reinterpret_cast<const void *>(fn), (int)pl.smem) != SS_OK ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, pl.W * 32, pl.smem) != cudaSuccess) {
         cudaGetLastError();
         return 0;

@@ -408,8 +408,7 @@ ss_status launch_shape(const S6Args &a, const WSPlan &pl, void *workspace, cudaS
     prm.dgroups = pl.dgroups;
     prm.timeout_ns = timeout_ns;
     auto kern = a.softplus ? s6_ws_kernel<IO, T, S, true> : s6_ws_kernel<IO, T, S, false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
-        cudaSuccess)
+    if (raise_smem_limit(reinterpret_cast<const void *>(kern), (int)pl.smem) != SS_OK)
         return SS_ERR_CUDA;
     kern<<<(unsigned)pl.ctas, S * 32, pl.smem, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? SS_OK : SS_ERR_CUDA;

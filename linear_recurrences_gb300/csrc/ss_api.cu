@@ -2,6 +2,9 @@
 // The arithmetic lives in affine_scan.cu and s6_scan.cu.
 #include <atomic>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "ss_common.cuh"
 #include "ss_internal.h"
@@ -72,6 +75,26 @@ ss_status affine_entry(const float *a, const float *b, float *h, int64_t n, void
 
 namespace ss {
 unsigned long long spin_timeout_ns() { return g_timeout_ns.load(); }
+
+ss_status raise_smem_limit(const void *fn, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> limits;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SS_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    int &cur = limits[{dev, fn}];
+    if (bytes <= cur) return SS_OK;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return SS_ERR_CUDA;
+    }
+    cur = bytes;
+    return SS_OK;
+}
 long long take_skip_unit() { return g_skip_unit.exchange(-1); }
 }  // namespace ss
 

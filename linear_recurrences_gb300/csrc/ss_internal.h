@@ -85,6 +85,12 @@ struct S6Args {
     int bidir;
 };
 
+// Raises the dynamic shared-memory limit of kernel `fn` on the current
+// device to at least `bytes` (a per-device attribute). The limit only ever
+// grows, under a lock, so a launch sized under an earlier call stays valid
+// while another host thread launches the same kernel with another size.
+ss_status raise_smem_limit(const void *fn, int bytes);
+
 // Current bound on device-side waits (ss_set_spin_timeout_ns).
 unsigned long long spin_timeout_ns();
 // Consumes a pending ss_testing_skip_publish_once request (-1 if none).
