@@ -413,9 +413,16 @@ def bench_proj_gemm(torch, ss, dev, steps, warmup, stream):
     peaks, kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", 1900.0))
     tf = flops / (ms * 1e-3) / 1e12
+    # for context, not a product path: the vendor library's plain bf16 GEMM
+    # (torch.mm, no bias) on the same operands and shape, timed the same way
+    WT = W.t()
+    lib_per, _ = time_launches(torch, lambda: torch.mm(x, WT, out=out), steps, warmup, stream)
+    lib_ms = statistics.mean(lib_per)
     return {"shape": [M, K, Nout], "ms": ms, "ms_min": min(per), "tflops": tf,
             "bound": "tensor", "peak_tflops": peak, "peak_source": f"{kind} bf16_tflops",
             "roofline_frac": tf / peak, "kernel": "proj_gemm_kernel (tcgen05, TMA, bias epilogue)",
+            "library_same_shape": {"what": "torch.mm bf16 (cuBLAS), no bias", "ms": lib_ms,
+                                   "tflops": flops / (lib_ms * 1e-3) / 1e12},
             "l2": "inputs (100 MB x + 4.8 MB W) near L2 size, no flush"}
 
 

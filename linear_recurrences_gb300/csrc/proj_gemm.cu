@@ -12,27 +12,36 @@
 //
 // Kernel (persistent, one CTA per SM, warp-specialised, 6 warps):
 //   warp 0    TMA producer: the A tile (128 rows of x, 64 K-columns) and the
-//             B tile (BN rows of W, 64 K-columns) of each K-block into a
+//             B tile (BN rows of W, or half of them in a pair, 64
+//             K-columns) of each K-block into a
 //             ring of shared-memory stages, both K-major with the 128-byte
 //             swizzle (one 128-byte row per tile row, 8-row atoms of 1 KB);
 //   warp 1    allocates 512 columns of tensor memory (two fp32 accumulators
 //             of 128 lanes x 256 columns) and, from one thread, issues
-//             tcgen05.mma (M = 128, N = BN, K = 16 per instruction, four per
-//             K-block); tcgen05.commit frees each stage when its MMAs have
+//             tcgen05.mma (M = 128, or 256 in a pair; N = BN, K = 16 per
+//             instruction, four per K-block); tcgen05.commit frees each
+//             stage when its MMAs have
 //             read it and hands a finished accumulator to the epilogue;
 //   warps 2-5 epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
 //             (tile rows), 32 columns per tcgen05.ld, adds the bias, rounds
 //             to bf16 and writes the 32 x 32 chunk to shared memory, from
 //             where one TMA tile store sends it to global memory.
 // With two accumulators the epilogue of one tile runs under the main loop
-// of the next. CTAs run in clusters of two on neighbouring SMs: the pair
-// takes two M-blocks of the same N-block at a time, each CTA loads its own
-// x tile and half of the shared W tile, multicast into both CTAs' shared
-// memory, so each W byte leaves L2 once per pair (a stage is refilled only
-// after both CTAs' MMAs have read it: each MMA thread's commit arrives on
-// both CTAs' stage barriers). Pairs take (M-block pair, N-block) tiles
-// round-robin, so the pairs working at one time share their x tiles through
-// L2; W stays in L2 throughout.
+// of the next. When there are two M-blocks or more, CTAs run in clusters of
+// two on neighbouring SMs and share one MMA of M = 256 (cta_group::2): the
+// pair takes two M-blocks of the same N-block at a time, each CTA loads its
+// own x tile and its half of the W tile (so a stage is A + BN/2 rows and
+// each W byte leaves L2 once per pair), and the leader's one thread issues
+// MMAs that read both CTAs' shared memory and accumulate into both CTAs'
+// tensor memory (each its 128 rows, all BN columns). Both CTAs' tile copies
+// complete on the leader's stage barrier (which the leader arms for the
+// pair's bytes); the leader's commits arrive on both CTAs' barriers (stage
+// free, accumulator full) and the epilogue warps of both release an
+// accumulator on the leader's barrier. Halving the W rows each SM stages and reads
+// halves the shared-memory traffic of W, which with M = 128 MMAs per SM
+// competes with the operand reads of the tensor cores. Pairs take
+// (M-block pair, N-block) tiles round-robin, so the pairs working at one
+// time share their x tiles through L2; W stays in L2 throughout.
 //
 // Every wait is bounded: on timeout the CTA records SS_ERR_TIMEOUT in the
 // workspace header, every role leaves its loop, the producer waits (bounded)
@@ -55,7 +64,8 @@ constexpr int kBK = 64;           // K-block: 64 bf16 = one 128-byte swizzled ro
 constexpr int kUmmaK = 16;        // K per tcgen05.mma with 16-bit inputs
 constexpr int kMaxBN = 256;       // UMMA N limit for M = 128
 constexpr int kAccCols = 256;     // tensor-memory columns per accumulator
-constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kAccs = 2;          // accumulators (the epilogue of one tile under the next's MMAs)
+constexpr int kTmemCols = kAccs * kAccCols;
 constexpr int kThreads = 192;     // producer warp, MMA warp, 4 epilogue warps
 constexpr int kMaxStages = 8;
 constexpr size_t kATileBytes = (size_t)kBM * kBK * 2;  // 16 KB
@@ -82,7 +92,7 @@ struct GemmShared {
     uint64_t full[kMaxStages];   // stage s holds its K-block (TMA complete_tx)
     uint64_t empty[kMaxStages];  // stage s was read by its MMAs (tcgen05.commit)
     uint64_t acc_full[2];        // accumulator a holds a finished tile
-    uint64_t acc_empty[2];       // accumulator a was read by the epilogue (4 warps)
+    uint64_t acc_empty[2];       // accumulator a was read by the epilogue (4 warps, 8 in a pair)
     uint64_t drain;              // the MMA thread's last MMAs completed
     uint32_t tmem_base;
     int abort;
@@ -119,23 +129,87 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
                  ::"r"(smem_addr(bar)) : "memory");
 }
 
-// As umma_commit, arriving on `bar` at the same offset in every CTA of the
-// cluster named in `mask`.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask) {
+// The CTA-pair forms (cta_group::2, one MMA of M = 256 over two SMs). Every
+// tcgen05 instruction of a kernel names the same group, so the pair kernel
+// uses these for its allocation, MMAs, commits and release throughout.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)), "h"(mask) : "memory");
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
-// 2D tile copy into `dst` (and the same offset) of every CTA of the cluster in
-// `mask`, completing on `bar` at the same offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const void *tmap, int x, int y,
-                                               uint64_t *bar, uint16_t mask) {
+// Arrives once on `bar`, at the same offset in both CTAs of the pair, when
+// every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)), "h"((uint16_t)0x3) : "memory");
+}
+
+template <bool TWO> __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t cols) {
+    if constexpr (TWO) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr(dst)), "r"(cols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_addr(dst)), "r"(cols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+}
+
+template <bool TWO> __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    if constexpr (TWO)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                     : "memory");
+}
+
+// Address of `p` (a shared variable of this CTA) in the CTA of cluster rank
+// `rank`, at the same offset.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, unsigned rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t caddr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
+// 2D tile copy into this CTA's `dst`, completing on the barrier at cluster
+// address `bar_cluster`, which may be in the other CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const void *tmap, int x, int y,
+                                                 uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2 [%0], [%1, {%2, %3}], [%4];"
         ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y),
-          "r"(smem_addr(bar)), "h"(mask) : "memory");
+          "r"(bar_cluster) : "memory");
+}
+
+// Arrival on a barrier of either CTA of the cluster, releasing at cluster
+// scope (this thread's earlier accesses are ordered before it for threads of
+// the other CTA that observe the phase complete).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
 }
 
 __device__ __forceinline__ void cluster_sync() {
@@ -182,12 +256,17 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, 
 
 // Waits for phase `parity` of `bar`; false once the CTA is aborting or the
 // wait outlived the launch's timeout (which starts the abort).
+// `cluster`: the phase is completed by arrivals from the other CTA of the
+// pair, whose earlier accesses the waiter must see (acquire at cluster scope).
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, unsigned parity, const GemmParams &p,
-                                              GemmShared &sh, unsigned where) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                              GemmShared &sh, unsigned where, bool cluster = false) {
+    auto try_wait = [&] {
+        return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (try_wait()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (unsigned it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait()) return true;
         if ((it & 255u) == 0u) {
             if (*reinterpret_cast<volatile int *>(&sh.abort)) return false;
             if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -200,50 +279,64 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, unsigned parity, co
 }
 
 // ---------------------------------------------------------------- kernel
-// PAIR: clusters of two CTAs sharing the W tile (see the top of the file);
-// otherwise every CTA loads its own tiles.
-template <bool PAIR>
+// TWO: clusters of two CTAs running one M = 256 MMA per K-step between them
+// (see the top of the file); otherwise every CTA runs its own M = 128 MMAs.
+template <bool TWO>
 __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ GemmShared sh;
-    // stages start on 1024-byte boundaries (the swizzle atom)
+    // stages start on 1024-byte boundaries (the swizzle atom), at the same
+    // offsets in both CTAs of a pair (the pair's MMAs address both by the
+    // leader's offsets)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const size_t stage_bytes = kATileBytes + (size_t)p.BN * kBK * 2;
+    const int b_rows = TWO ? p.BN / 2 : p.BN;  // W rows of a stage held by this CTA
+    const size_t stage_bytes = kATileBytes + (size_t)b_rows * kBK * 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // work units: (M-block, N-block) tiles, or (M-block pair, N-block) per cluster
-    const unsigned rank = PAIR ? cluster_rank() : 0u;
-    const long long unit0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
-    const long long unit_step = PAIR ? gridDim.x / 2 : gridDim.x;
-    auto m_block = [&](long long u) { return PAIR ? 2 * (u / p.n_tiles_n) + rank : u / p.n_tiles_n; };
+    const unsigned rank = TWO ? cluster_rank() : 0u;
+    const long long unit0 = TWO ? blockIdx.x / 2 : blockIdx.x;
+    const long long unit_step = TWO ? gridDim.x / 2 : gridDim.x;
+    auto m_block = [&](long long u) { return TWO ? 2 * (u / p.n_tiles_n) + rank : u / p.n_tiles_n; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], PAIR ? 2 : 1);
+            mbar_init(&sh.empty[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&sh.acc_full[a], 1);
-            mbar_init(&sh.acc_empty[a], 4);
+            mbar_init(&sh.acc_empty[a], TWO ? 8 : 4);  // the epilogue warps (of both CTAs)
         }
         mbar_init(&sh.drain, 1);
         sh.abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_addr(&sh.tmem_base)), "r"(kTmemCols) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        // a pair allocates collectively: the same columns in both CTAs
+        tmem_alloc<TWO>(&sh.tmem_base, kTmemCols);
         tc_fence_before();
     }
-    if (PAIR)
-        cluster_sync();  // the peer's barriers are initialised before any multicast
+    if (TWO)
+        cluster_sync();  // both CTAs' barriers initialised, both allocations made
     else
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    bool run = true;
+    if (TWO) {
+        // the pair's MMAs write both CTAs' tensor memory at the leader's
+        // address: a pair whose columns differ does no work (both CTAs see
+        // the same two addresses, so both decide alike)
+        const uint32_t other = ld_cluster_u32(cluster_addr(&sh.tmem_base, rank ^ 1u));
+        if (other != tmem) {
+            run = false;
+            if (threadIdx.x == 0) record_error(p.ws, SS_ERR_CUDA, 5u, 6u, blockIdx.x);
+        }
+    }
 
-    if (warp == 0) {
+    if (!run) {
+    } else if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             int stage = 0;
@@ -259,13 +352,18 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                         break;
                     }
                     uint8_t *sa = smem + stage * stage_bytes;
-                    mbar_arrive_expect_tx(&sh.full[stage], (unsigned)stage_bytes);
-                    tma_load_2d(sa, &p.tm_a, kb * kBK, m0, &sh.full[stage]);
-                    if (PAIR) {  // this CTA's half of the W tile, into both CTAs
-                        const int half = p.BN / 2;
-                        tma_load_2d_mc(sa + kATileBytes + (size_t)rank * half * kBK * 2, &p.tm_b,
-                                       kb * kBK, n0 + (int)rank * half, &sh.full[stage], 0x3);
+                    if constexpr (TWO) {
+                        // both CTAs' copies complete on the leader's barrier,
+                        // which the leader arms for the pair's bytes
+                        const uint32_t fb = cluster_addr(&sh.full[stage], 0);
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(&sh.full[stage], 2u * (unsigned)stage_bytes);
+                        tma_load_2d_pair(sa, &p.tm_a, kb * kBK, m0, fb);
+                        tma_load_2d_pair(sa + kATileBytes, &p.tm_b, kb * kBK, n0 + (int)rank * b_rows,
+                                         fb);
                     } else {
+                        mbar_arrive_expect_tx(&sh.full[stage], (unsigned)stage_bytes);
+                        tma_load_2d(sa, &p.tm_a, kb * kBK, m0, &sh.full[stage]);
                         tma_load_2d(sa + kATileBytes, &p.tm_b, kb * kBK, n0, &sh.full[stage]);
                     }
                     ++issued;
@@ -276,14 +374,18 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                 }
             }
             // the last copy into each stage has landed before the CTA leaves
-            // (immediate unless the CTA is aborting)
+            // (immediate unless the CTA is aborting); a pair's copies all
+            // complete on the leader's barriers, and the other CTA does not
+            // leave before the leader (the cluster barrier at the end)
             const long long first = issued > p.stages ? issued - p.stages : 0;
-            for (long long i = first; i < issued; ++i)
-                mbar_wait_bounded(&sh.full[i % p.stages], (unsigned)((i / p.stages) & 1), p.timeout_ns);
+            if (!TWO || rank == 0)
+                for (long long i = first; i < issued; ++i)
+                    mbar_wait_bounded(&sh.full[i % p.stages], (unsigned)((i / p.stages) & 1),
+                                      p.timeout_ns);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && (!TWO || rank == 0)) {
+            // -------------------------------------------- MMA issuer
             int stage = 0;
             unsigned phase = 0;
             int acc = 0;
@@ -291,10 +393,14 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
             bool ok = true;
             const uint32_t smem0 = smem_addr(smem);
             for (long long u = unit0; ok && u < p.num_tiles; u += unit_step) {
-                if (!wait_or_abort(&sh.acc_empty[acc], acc_phase ^ 1u, p, sh, 2u)) break;
+                if (!wait_or_abort(&sh.acc_empty[acc], acc_phase ^ 1u, p, sh, 2u, TWO)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(acc * kAccCols);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    // the stage landed (in a pair: in both CTAs; the copies'
+                    // completion on this barrier is what orders their data
+                    // before the MMAs, as for a single CTA, so a CTA-scope
+                    // wait suffices and measured 1% faster than cluster scope)
                     if (!wait_or_abort(&sh.full[stage], phase, p, sh, 3u)) {
                         ok = false;
                         break;
@@ -303,12 +409,17 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                     const uint32_t sa = smem0 + (uint32_t)(stage * stage_bytes);
                     const uint32_t sb = sa + (uint32_t)kATileBytes;
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k)
-                        umma_bf16(d_tmem, sw128_desc(sa + k * kUmmaK * 2),
-                                  sw128_desc(sb + k * kUmmaK * 2), p.idesc, (kb | k) != 0);
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t ad = sw128_desc(sa + k * kUmmaK * 2);
+                        const uint64_t bd = sw128_desc(sb + k * kUmmaK * 2);
+                        if constexpr (TWO)
+                            umma_bf16_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                        else
+                            umma_bf16(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
+                    }
                     // stage free once these MMAs read it (in both CTAs of a pair)
-                    if (PAIR)
-                        umma_commit_mc(&sh.empty[stage], 0x3);
+                    if constexpr (TWO)
+                        umma_commit_pair(&sh.empty[stage]);
                     else
                         umma_commit(&sh.empty[stage]);
                     if (++stage == p.stages) {
@@ -317,13 +428,24 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                     }
                 }
                 if (!ok) break;
-                umma_commit(&sh.acc_full[acc]);  // tile done: hand it to the epilogue
-                if (++acc == 2) {
+                // tile done: hand it to the epilogue (of both CTAs)
+                if constexpr (TWO)
+                    umma_commit_pair(&sh.acc_full[acc]);
+                else
+                    umma_commit(&sh.acc_full[acc]);
+                if (++acc == kAccs) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
-            umma_commit(&sh.drain);
+            if constexpr (TWO)
+                umma_commit_pair(&sh.drain);
+            else
+                umma_commit(&sh.drain);
+            mbar_wait_bounded(&sh.drain, 0u, p.timeout_ns);
+        } else if (TWO && lane == 0) {
+            // the other CTA of a pair: the leader's MMAs write this CTA's
+            // tensor memory, and have completed before it is released
             mbar_wait_bounded(&sh.drain, 0u, p.timeout_ns);
         }
     } else {
@@ -336,6 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         const int quarter = warp & 3;  // tensor-memory lanes 32 quarter .. + 31
         uint4 *stg = reinterpret_cast<uint4 *>(smem + (size_t)p.stages * stage_bytes) +
                      (size_t)(warp - 2) * 2 * 128;
+        // the accumulator's release goes to the MMA thread's CTA
+        const uint32_t acc_empty0 = TWO ? cluster_addr(&sh.acc_empty[0], 0) : 0u;
         unsigned chunk_no = 0;
         int acc = 0;
         unsigned acc_phase = 0;
@@ -386,8 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
             // the accumulator is free once every lane's loads have completed
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.acc_empty[acc]);
-            if (++acc == 2) {
+            if (lane == 0) {
+                if constexpr (TWO)
+                    mbar_arrive_cluster(acc_empty0 + (uint32_t)(acc * sizeof(uint64_t)));
+                else
+                    mbar_arrive(&sh.acc_empty[acc]);
+            }
+            if (++acc == kAccs) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -395,14 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         if (lane == 0) bulk_wait<0>();  // every store has left shared memory
     }
     __syncthreads();
+    // neither CTA of a pair releases its tensor memory or leaves while the
+    // other may still arrive on its barriers
+    if (TWO) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
-                     ::"r"(tmem), "r"(kTmemCols) : "memory");
+        tmem_dealloc<TWO>(tmem, kTmemCols);
     }
-    // neither CTA of a pair leaves while the other may still multicast into
-    // its shared memory or arrive on its barriers
-    if (PAIR) cluster_sync();
 }
 
 // ---------------------------------------------------------------- planning
@@ -423,7 +551,8 @@ GemmPlan plan_gemm(int64_t M, int64_t K, int64_t Nout) {
     // pairs need two M-blocks and W half-tiles of whole 8-row swizzle atoms
     g.pair = m_tiles >= 2 && (g.BN / 2) % 8 == 0;
     g.num_tiles = (g.pair ? (m_tiles + 1) / 2 : m_tiles) * g.n_tiles_n;
-    const size_t stage_bytes = kATileBytes + (size_t)g.BN * kBK * 2;
+    // a pair's CTAs each hold half of the W tile
+    const size_t stage_bytes = kATileBytes + (size_t)(g.pair ? g.BN / 2 : g.BN) * kBK * 2;
     g.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - 1024 - kStagingBytes) / stage_bytes);
     g.smem = 1024 + (size_t)g.stages * stage_bytes + kStagingBytes;
     return g;
@@ -541,9 +670,10 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
     prm.n_tiles_n = g.n_tiles_n;
     // kind::f16 descriptor: fp32 accumulator (bits 4-5 = 1), bf16 A and B
     // (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits
-    // 17-22, M >> 4 in bits 24-28
+    // 17-22, M >> 4 in bits 24-28 (M = 256 for a pair's MMA)
+    const unsigned mma_m = g.pair ? 2 * kBM : kBM;
     prm.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((unsigned)(g.BN >> 3) << 17) |
-                ((unsigned)(kBM >> 4) << 24);
+                ((mma_m >> 4) << 24);
     LaunchInfo li;
     const ss_status st = launch_info(g.smem, &li);
     if (st != SS_OK) return st;
