@@ -11,15 +11,15 @@
 // here does the same.
 //
 // Kernel (persistent, one CTA per SM, warp-specialised, 6 warps):
-//   warp 0    TMA producer: the A tile (128 rows of x, 64 K-columns) and the
-//             B tile (BN rows of W, or half of them in a pair, 64
-//             K-columns) of each K-block into a
-//             ring of shared-memory stages, both K-major with the 128-byte
-//             swizzle (one 128-byte row per tile row, 8-row atoms of 1 KB);
+//   warp 0    TMA producer: the A tile (128 rows of x) and the B tile (BN
+//             rows of W, or half of them in a pair) of each 128-column
+//             K-block, as two 64-column boxes each, into a ring of
+//             shared-memory stages, both K-major with the 128-byte swizzle
+//             (one 128-byte row per box row, 8-row atoms of 1 KB);
 //   warp 1    allocates 512 columns of tensor memory (two fp32 accumulators
 //             of 128 lanes x 256 columns) and, from one thread, issues
 //             tcgen05.mma (M = 128, or 256 in a pair; N = BN, K = 16 per
-//             instruction, four per K-block); tcgen05.commit frees each
+//             instruction, eight per K-block); tcgen05.commit frees each
 //             stage when its MMAs have
 //             read it and hands a finished accumulator to the epilogue;
 //   warps 2-5 epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
@@ -60,7 +60,8 @@ namespace ss {
 namespace {
 
 constexpr int kBM = 128;          // tile rows (UMMA M)
-constexpr int kBK = 64;           // K-block: 64 bf16 = one 128-byte swizzled row
+constexpr int kBK = 64;           // K-box: 64 bf16 = one 128-byte swizzled row
+constexpr int kSub = 2;           // K-boxes per stage: 128 K-columns per barrier round trip
 constexpr int kUmmaK = 16;        // K per tcgen05.mma with 16-bit inputs
 constexpr int kMaxBN = 256;       // UMMA N limit for M = 128
 constexpr int kAccCols = 256;     // tensor-memory columns per accumulator
@@ -291,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int b_rows = TWO ? p.BN / 2 : p.BN;  // W rows of a stage held by this CTA
-    const size_t stage_bytes = kATileBytes + (size_t)b_rows * kBK * 2;
+    const size_t b_box = (size_t)b_rows * kBK * 2;  // one K-box of this CTA's W rows
+    const size_t stage_bytes = kSub * (kATileBytes + b_box);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // work units: (M-block, N-block) tiles, or (M-block pair, N-block) per cluster
     const unsigned rank = TWO ? cluster_rank() : 0u;
@@ -358,13 +360,22 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                         const uint32_t fb = cluster_addr(&sh.full[stage], 0);
                         if (rank == 0)
                             mbar_arrive_expect_tx(&sh.full[stage], 2u * (unsigned)stage_bytes);
-                        tma_load_2d_pair(sa, &p.tm_a, kb * kBK, m0, fb);
-                        tma_load_2d_pair(sa + kATileBytes, &p.tm_b, kb * kBK, n0 + (int)rank * b_rows,
-                                         fb);
+#pragma unroll
+                        for (int j = 0; j < kSub; ++j) {
+                            const int x = (kb * kSub + j) * kBK;
+                            tma_load_2d_pair(sa + j * kATileBytes, &p.tm_a, x, m0, fb);
+                            tma_load_2d_pair(sa + kSub * kATileBytes + j * b_box, &p.tm_b, x,
+                                             n0 + (int)rank * b_rows, fb);
+                        }
                     } else {
                         mbar_arrive_expect_tx(&sh.full[stage], (unsigned)stage_bytes);
-                        tma_load_2d(sa, &p.tm_a, kb * kBK, m0, &sh.full[stage]);
-                        tma_load_2d(sa + kATileBytes, &p.tm_b, kb * kBK, n0, &sh.full[stage]);
+#pragma unroll
+                        for (int j = 0; j < kSub; ++j) {
+                            const int x = (kb * kSub + j) * kBK;
+                            tma_load_2d(sa + j * kATileBytes, &p.tm_a, x, m0, &sh.full[stage]);
+                            tma_load_2d(sa + kSub * kATileBytes + j * b_box, &p.tm_b, x, n0,
+                                        &sh.full[stage]);
+                        }
                     }
                     ++issued;
                     if (++stage == p.stages) {
@@ -407,16 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                     }
                     tc_fence_after();
                     const uint32_t sa = smem0 + (uint32_t)(stage * stage_bytes);
-                    const uint32_t sb = sa + (uint32_t)kATileBytes;
+                    const uint32_t sb = sa + (uint32_t)(kSub * kATileBytes);
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t ad = sw128_desc(sa + k * kUmmaK * 2);
-                        const uint64_t bd = sw128_desc(sb + k * kUmmaK * 2);
-                        if constexpr (TWO)
-                            umma_bf16_pair(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-                        else
-                            umma_bf16(d_tmem, ad, bd, p.idesc, (kb | k) != 0);
-                    }
+                    for (int j = 0; j < kSub; ++j)
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            const uint64_t ad =
+                                sw128_desc(sa + (uint32_t)(j * kATileBytes) + k * kUmmaK * 2);
+                            const uint64_t bd =
+                                sw128_desc(sb + (uint32_t)(j * b_box) + k * kUmmaK * 2);
+                            const uint32_t accum = (kb | j | k) != 0;
+                            if constexpr (TWO)
+                                umma_bf16_pair(d_tmem, ad, bd, p.idesc, accum);
+                            else
+                                umma_bf16(d_tmem, ad, bd, p.idesc, accum);
+                        }
                     // stage free once these MMAs read it (in both CTAs of a pair)
                     if constexpr (TWO)
                         umma_commit_pair(&sh.empty[stage]);
@@ -546,13 +562,13 @@ GemmPlan plan_gemm(int64_t M, int64_t K, int64_t Nout) {
     g.n_tiles_n = (int)((Nout + kMaxBN - 1) / kMaxBN);
     const int64_t per = (Nout + g.n_tiles_n - 1) / g.n_tiles_n;
     g.BN = (int)((per + 31) / 32 * 32);
-    g.k_blocks = (int)((K + kBK - 1) / kBK);
+    g.k_blocks = (int)((K + kSub * kBK - 1) / (kSub * kBK));
     const int64_t m_tiles = (M + kBM - 1) / kBM;
     // pairs need two M-blocks and W half-tiles of whole 8-row swizzle atoms
     g.pair = m_tiles >= 2 && (g.BN / 2) % 8 == 0;
     g.num_tiles = (g.pair ? (m_tiles + 1) / 2 : m_tiles) * g.n_tiles_n;
     // a pair's CTAs each hold half of the W tile
-    const size_t stage_bytes = kATileBytes + (size_t)(g.pair ? g.BN / 2 : g.BN) * kBK * 2;
+    const size_t stage_bytes = kSub * (kATileBytes + (size_t)(g.pair ? g.BN / 2 : g.BN) * kBK * 2);
     g.stages = (int)std::min<size_t>(kMaxStages, (kSmemBudget - 1024 - kStagingBytes) / stage_bytes);
     g.smem = 1024 + (size_t)g.stages * stage_bytes + kStagingBytes;
     return g;
