@@ -76,7 +76,7 @@ constexpr size_t kStagingBytes = 4 * 2 * 32 * 32 * 2;  // epilogue: 2 buffers of
 struct GemmParams {
     CUtensorMap tm_a;    // x as (K, M) bf16, box (64, 128), 128-byte swizzle
     CUtensorMap tm_b;    // W as (K, Nout) bf16, box (64, BN), 128-byte swizzle
-    CUtensorMap tm_out;  // out as (Nout, M) bf16, row stride ld_out, box (32, 32)
+    CUtensorMap tm_out;  // out as (Nout, M) bf16, row stride ld_out, box (32, 32), 64-byte swizzle
     __nv_bfloat16 *out;  // (M, ld_out) row-major
     const float *bias;   // (n_bias,) or null
     long long M;
@@ -470,7 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
         // warp's two 2 KB staging buffers in shared memory (its 32 rows x 64
         // bytes) and leaves as one TMA tile store, clipped at M and Nout, so
         // whole row segments reach L2 and the lanes move on while the copy
-        // runs.
+        // runs. The buffer holds the chunk in the store's 64-byte swizzle
+        // (16-byte piece q of row r at position q ^ ((r >> 1) & 3)), so the
+        // 8 rows of each 16-byte store phase fall in distinct banks.
         const int quarter = warp & 3;  // tensor-memory lanes 32 quarter .. + 31
         uint4 *stg = reinterpret_cast<uint4 *>(smem + (size_t)p.stages * stage_bytes) +
                      (size_t)(warp - 2) * 2 * 128;
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) proj_gemm_kernel(const __grid_con
                     w.y = *reinterpret_cast<uint32_t *>(&h1);
                     w.z = *reinterpret_cast<uint32_t *>(&h2);
                     w.w = *reinterpret_cast<uint32_t *>(&h3);
-                    buf[lane * 4 + q] = w;
+                    buf[lane * 4 + (q ^ ((lane >> 1) & 3))] = w;
                 }
                 fence_proxy_async_smem();  // visible to the tensor copy
                 __syncwarp();
@@ -667,7 +669,7 @@ ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float 
         const uint64_t dims[2] = {(uint64_t)Nout, (uint64_t)M};
         const uint64_t strides[1] = {(uint64_t)ld_out * 2};
         const uint32_t box[2] = {32u, 32u};
-        if (!encode_tiled_map(&prm.tm_out, out, true, 2, dims, strides, box))
+        if (!encode_tiled_map(&prm.tm_out, out, true, 2, dims, strides, box, 64))
             return SS_ERR_UNSUPPORTED;
     }
     prm.out = static_cast<__nv_bfloat16 *>(out);
