@@ -71,6 +71,17 @@ int ss_testing_proj_gemm(const void *x, const void *W, void *out, const float *b
                          int64_t n_bias, int64_t M, int64_t K, int64_t Nout, int64_t ld_out,
                          void *workspace, void *stream);
 
+/*
+ * Describes the launch plan of ss_testing_proj_gemm (and of the bf16 layer's
+ * projections) for an M x K by Nout x K product, on the host, without a GPU:
+ * out = eight host int64 values {N-tile width BN, N-tiles, K-columns per
+ * shared-memory stage, K-blocks, stages, 1 if CTA pairs share one M = 256
+ * MMA (two M-blocks or more) else 0, work units (tiles, or tile pairs),
+ * dynamic shared memory bytes per CTA}. Returns 0, or -1 for a shape with a
+ * size <= 0 or above 2^31 - 1, or a null out.
+ */
+int ss_testing_proj_gemm_describe_plan(int64_t M, int64_t K, int64_t Nout, int64_t *out);
+
 #ifdef __cplusplus
 }
 #endif

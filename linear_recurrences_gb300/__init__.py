@@ -27,6 +27,7 @@ __all__ = [
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_testing_s6_plan", "ss_testing_s6_describe_plan", "ss_testing_proj_gemm",
+    "ss_testing_proj_gemm_describe_plan",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_affine_scan_noalloc_status",
     "SS_AFFINE_NOALLOC_MAX_N",
     "ss_selective_scan_fwd_state", "ss_selective_scan_bwd", "ss_selective_scan_bwd_workspace_bytes",
@@ -44,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "ss_selective_scan_workspace_bytes", "ss_selective_scan_fwd", "ss_selective_scan_bidir",
     "ss_get_device_status", "ss_set_spin_timeout_ns", "ss_testing_skip_publish_once",
     "ss_testing_s6_plan", "ss_testing_s6_describe_plan", "ss_testing_proj_gemm",
+    "ss_testing_proj_gemm_describe_plan",
     "ss_probe_mufu_ex2", "ss_affine_scan_noalloc", "ss_affine_scan_noalloc_status",
     "ss_selective_scan_fwd_state",
     "ss_selective_scan_bwd_workspace_bytes", "ss_selective_scan_bwd",
@@ -113,6 +115,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.ss_testing_s6_describe_plan.restype = ci
     L.ss_testing_proj_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp]
     L.ss_testing_proj_gemm.restype = ci
+    L.ss_testing_proj_gemm_describe_plan.argtypes = [i64, i64, i64, ctypes.POINTER(ctypes.c_int64)]
+    L.ss_testing_proj_gemm_describe_plan.restype = ci
     L.ss_probe_mufu_ex2.argtypes = [vp, ci, ci, vp]
     L.ss_probe_mufu_ex2.restype = ci
     L.ss_affine_scan_noalloc.argtypes = [vp, vp, vp, i64, vp]
@@ -186,6 +190,17 @@ def ss_testing_s6_describe_plan(B, L, D, N, io_dtype=SS_F32, bidir=False):
     k = lib().ss_testing_s6_describe_plan(int(B), int(L), int(D), int(N), int(io_dtype),
                                           int(bool(bidir)), out)
     return k, tuple(out)
+
+
+def ss_testing_proj_gemm_describe_plan(M, K, Nout):
+    """Launch plan of the projection GEMM for an M x K by Nout x K product,
+    computed on the host: (N-tile width, N-tiles, K-columns per stage,
+    K-blocks, stages, pair (1/0), work units, dynamic shared memory bytes),
+    or None for an invalid shape."""
+    out = (ctypes.c_int64 * 8)()
+    if lib().ss_testing_proj_gemm_describe_plan(int(M), int(K), int(Nout), out) != 0:
+        return None
+    return tuple(out)
 
 
 def ss_testing_proj_gemm(x, W, bias=None, out=None, ld_out=None, workspace=None, stream=None):

@@ -636,6 +636,22 @@ ss_status launch_info(size_t smem, LaunchInfo *out) {
 
 }  // namespace
 
+int proj_gemm_describe_plan(int64_t M, int64_t K, int64_t Nout, int64_t *out) {
+    if (!out || M <= 0 || K <= 0 || Nout <= 0 || M > 0x7fffffffLL || K > 0x7fffffffLL ||
+        Nout > 0x7fffffffLL)
+        return -1;
+    const GemmPlan g = plan_gemm(M, K, Nout);
+    out[0] = g.BN;
+    out[1] = g.n_tiles_n;
+    out[2] = (int64_t)kSub * kBK;  // K-columns per stage
+    out[3] = g.k_blocks;
+    out[4] = g.stages;
+    out[5] = g.pair ? 1 : 0;
+    out[6] = g.num_tiles;
+    out[7] = (int64_t)g.smem;
+    return 0;
+}
+
 bool proj_gemm_supported(const void *x, const void *W, const void *out, int64_t M, int64_t K,
                          int64_t Nout, int64_t ld_out) {
     auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };

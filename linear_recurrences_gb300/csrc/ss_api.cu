@@ -306,6 +306,10 @@ int ss_testing_proj_gemm(const void *x, const void *W, void *out, const float *b
                                 static_cast<cudaStream_t>(stream), g_timeout_ns.load());
 }
 
+int ss_testing_proj_gemm_describe_plan(int64_t M, int64_t K, int64_t Nout, int64_t *out) {
+    return ss::proj_gemm_describe_plan(M, K, Nout, out);
+}
+
 int ss_testing_s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int io_dtype,
                                 int bidir, int64_t *out) {
     if (!out || (io_dtype != SS_F32 && io_dtype != SS_BF16)) return -1;

@@ -54,6 +54,10 @@ bool proj_gemm_supported(const void *x, const void *W, const void *out, int64_t 
 ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float *bias,
                            int64_t n_bias, int64_t M, int64_t K, int64_t Nout, int64_t ld_out,
                            void *workspace, cudaStream_t stream, unsigned long long timeout_ns);
+// The launch plan of a GEMM of this shape (host only, no GPU needed): out =
+// {BN, N-tiles, K-columns per stage, K-blocks, stages, pair (1 or 0), work
+// units, dynamic shared memory bytes}; -1 for an invalid shape.
+int proj_gemm_describe_plan(int64_t M, int64_t K, int64_t Nout, int64_t *out);
 
 size_t affine_workspace_bytes(int64_t n);
 // log_step_tiles: scan each tile with the log-step (Hillis-Steele) algorithm

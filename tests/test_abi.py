@@ -255,3 +255,28 @@ def test_backward_plans_fill_whole_waves(L):
     gradient CTAs per SM on 152 SMs: 2 for the fp32 workload, 7 for bf16."""
     assert _bwd_ranges(L, 16, 2048, 256, 16) == 2
     assert _bwd_ranges(L, 8, 4096, 1536, 16) == 7
+
+
+def test_projection_gemm_plans(L):
+    """The projection GEMM's planner (host only): the layer's shape takes
+    7 N-tiles of 224 columns, 12 K-blocks of 128 columns in 3 stages and CTA
+    pairs; over a sweep of shapes every plan covers the product with no
+    empty tile, has at least two stages, fits in shared memory, and pairs
+    CTAs exactly when there are two M-blocks or more."""
+    assert ss.ss_testing_proj_gemm_describe_plan(32768, 1536, 1568) == \
+        (224, 7, 128, 12, 3, 1, 896, 201728)
+    for M in (1, 100, 128, 129, 256, 300, 32768, 1000003):
+        for K in (8, 40, 64, 72, 128, 1536, 4096):
+            for Nout in (8, 50, 224, 256, 257, 1568, 4096, 5000):
+                BN, nt, kc, kb, stages, pair, units, smem = \
+                    ss.ss_testing_proj_gemm_describe_plan(M, K, Nout)
+                assert BN % 32 == 0 and 32 <= BN <= 256
+                assert nt * BN >= Nout and (nt - 1) * BN < Nout
+                assert kb * kc >= K and (kb - 1) * kc < K
+                assert 2 <= stages <= 8
+                assert smem <= 224 * 1024
+                m_tiles = -(-M // 128)
+                assert pair == (1 if m_tiles >= 2 else 0)
+                assert units == (-(-m_tiles // 2) if pair else m_tiles) * nt
+    assert ss.ss_testing_proj_gemm_describe_plan(0, 64, 64) is None
+    assert ss.ss_testing_proj_gemm_describe_plan(64, -1, 64) is None
