@@ -282,7 +282,8 @@ ss_status ss_selective_scan_fwd_state(const void *x, const void *delta,
  * bias, the pre-activation is the product plus b_delta rounded once to
  * io_dtype: for SS_BF16 the library's tensor-core GEMM adds the bias to the
  * fp32 accumulator before the one rounding to bf16 (D must be a multiple of
- * 8, x and W_proj 16-byte aligned, else SS_ERR_UNSUPPORTED); for SS_F32 a
+ * 8, x and W_proj 16-byte aligned and B*L at most 2^31 - 256, else
+ * SS_ERR_UNSUPPORTED); for SS_F32 a
  * cuBLASLt fp32 GEMM writes the product and the scan adds the bias in fp32.
  * The workspace (ss_selective_scan_layer_workspace_bytes) holds the
  * projections, any GEMM scratch and the scan's workspace (first, so

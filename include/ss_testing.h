@@ -64,8 +64,9 @@ int ss_testing_s6_describe_plan(int64_t B, int64_t L, int64_t D, int64_t N, int 
  * as 16-byte tile stores); columns from there to ld_out are left untouched.
  * workspace: a zero-filled device block of at least 256 bytes (its header
  * takes device errors, read with ss_get_device_status). Returns
- * SS_ERR_UNSUPPORTED unless K and ld_out are multiples of 8, ld_out >= Nout
- * and x, W, out are 16-byte aligned. Asynchronous on `stream`.
+ * SS_ERR_UNSUPPORTED unless K and ld_out are multiples of 8, ld_out >= Nout,
+ * M, K and Nout are at most 2^31 - 256 (tile coordinates are 32-bit) and x,
+ * W, out are 16-byte aligned. Asynchronous on `stream`.
  */
 int ss_testing_proj_gemm(const void *x, const void *W, void *out, const float *bias,
                          int64_t n_bias, int64_t M, int64_t K, int64_t Nout, int64_t ld_out,
@@ -78,7 +79,7 @@ int ss_testing_proj_gemm(const void *x, const void *W, void *out, const float *b
  * shared-memory stage, K-blocks, stages, 1 if CTA pairs share one M = 256
  * MMA (two M-blocks or more) else 0, work units (tiles, or tile pairs),
  * dynamic shared memory bytes per CTA}. Returns 0, or -1 for a shape with a
- * size <= 0 or above 2^31 - 1, or a null out.
+ * size <= 0 or above 2^31 - 256, or a null out.
  */
 int ss_testing_proj_gemm_describe_plan(int64_t M, int64_t K, int64_t Nout, int64_t *out);
 

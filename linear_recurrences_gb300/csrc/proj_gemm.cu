@@ -72,6 +72,7 @@ constexpr int kMaxStages = 8;
 constexpr size_t kATileBytes = (size_t)kBM * kBK * 2;  // 16 KB
 constexpr size_t kSmemBudget = 224 * 1024;             // dynamic, incl. 1 KB alignment slack
 constexpr size_t kStagingBytes = 4 * 2 * 32 * 32 * 2;  // epilogue: 2 buffers of 32 x 32 bf16 per warp
+constexpr int64_t kMaxExtent = 0x7fffff00LL;  // M, K, Nout: int32 tile coordinates stay in range
 
 struct GemmParams {
     CUtensorMap tm_a;    // x as (K, M) bf16, box (64, 128), 128-byte swizzle
@@ -637,8 +638,8 @@ ss_status launch_info(size_t smem, LaunchInfo *out) {
 }  // namespace
 
 int proj_gemm_describe_plan(int64_t M, int64_t K, int64_t Nout, int64_t *out) {
-    if (!out || M <= 0 || K <= 0 || Nout <= 0 || M > 0x7fffffffLL || K > 0x7fffffffLL ||
-        Nout > 0x7fffffffLL)
+    if (!out || M <= 0 || K <= 0 || Nout <= 0 || M > kMaxExtent || K > kMaxExtent ||
+        Nout > kMaxExtent)
         return -1;
     const GemmPlan g = plan_gemm(M, K, Nout);
     out[0] = g.BN;
@@ -655,9 +656,10 @@ int proj_gemm_describe_plan(int64_t M, int64_t K, int64_t Nout, int64_t *out) {
 bool proj_gemm_supported(const void *x, const void *W, const void *out, int64_t M, int64_t K,
                          int64_t Nout, int64_t ld_out) {
     auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    // tile coordinates are 32-bit and run up to a tile past each extent
     return M > 0 && K > 0 && Nout > 0 && K % 8 == 0 && ld_out % 8 == 0 && ld_out >= Nout &&
-           M <= 0x7fffffffLL && K <= 0x7fffffffLL && Nout <= 0x7fffffffLL && al16(x) &&
-           al16(W) && al16(out);
+           M <= kMaxExtent && K <= kMaxExtent && Nout <= kMaxExtent && al16(x) && al16(W) &&
+           al16(out);
 }
 
 ss_status proj_gemm_launch(const void *x, const void *W, void *out, const float *bias,

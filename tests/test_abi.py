@@ -280,3 +280,12 @@ def test_projection_gemm_plans(L):
                 assert units == (-(-m_tiles // 2) if pair else m_tiles) * nt
     assert ss.ss_testing_proj_gemm_describe_plan(0, 64, 64) is None
     assert ss.ss_testing_proj_gemm_describe_plan(64, -1, 64) is None
+
+
+def test_projection_gemm_extent_limit(L):
+    """Tile coordinates are 32-bit: extents up to 2^31 - 256 plan, larger ones
+    are refused."""
+    assert ss.ss_testing_proj_gemm_describe_plan(2**31 - 256, 64, 64) is not None
+    assert ss.ss_testing_proj_gemm_describe_plan(2**31 - 255, 64, 64) is None
+    assert ss.ss_testing_proj_gemm_describe_plan(64, 2**31 - 255, 64) is None
+    assert ss.ss_testing_proj_gemm_describe_plan(64, 64, 2**31 - 255) is None
